@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of ragged paged attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference] [--no-cpu-baseline]
+
+One step = one rpa_forward over one synthetic batch (planner, decode kernel,
+prefill kernel; the page write is fused into the two attention kernels).
+Inputs are resident in HBM when the timed region starts; L2 is flushed (a
+256 MB write) before every timed step, outside its events.  Each step is timed
+with CUDA events on the launching stream, and each kernel inside it with the
+events rpa_forward_timed records.  With N > 1 (torchrun) every rank runs an
+independent replica ("replicas only": the op has no exchange step), the time
+is the max over ranks, and value counts the tokens of all ranks.
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead
+(on the host cores, a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ragged_paged_attention_kv_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "RPA tokens/s; decode KV HBM GB/s & prefill TFLOP/s vs GB300 peak"
+L2_FLUSH_BYTES = 256 << 20
+
+DESCRIPTIONS = {
+    "decode": "decode-heavy, Llama-3-8B attention shape: 256 seqs q_len=1, kv_len~U[512,4096]; "
+              "Hq32/Hkv8/D128, bf16 cache, page_size 16, 80000-page pool",
+    "mixed": "chunked-prefill mixed batch: 128 decode (kv~U[1024,8192]) + 8x512-token chunks "
+             "(prior kv~U[0,4096]) + 2x1536 fresh; Hq64/Hkv8/D128, bf16, page_size 32",
+    "long": "long-context prefill: 2 seqs q=kv=32768 causal; Hq32/Hkv8/D128, bf16, page_size 64",
+    "long_w4096": "long-context prefill: 2 seqs q=kv=32768, sliding_window 4096; "
+                  "Hq32/Hkv8/D128, bf16, page_size 64",
+    "fp8": "fp8 e4m3 cache (k/v scale 0.05), soft cap 30, sinks, window 128: 512 decode "
+           "(kv~U[256,16384]) + 8x256 chunks (prior kv~U[0,8192]); Hq64/Hkv8/D64, page_size 16",
+    "decode_small": "decode shape at 64 seqs (profiling size): q_len=1, kv_len~U[512,4096]; "
+                    "Hq32/Hkv8/D128, bf16, page_size 16, pool = pages used + 10%",
+    "tiny": "tiny mixed batch: 3 seqs (1,17),(24,24),(5,40); Hq4/Hkv2/D64/P16",
+}
+
+
+# ------------------------------------------------------------ work counting
+def classify(w):
+    """Per sequence: True where the planner takes the decode path."""
+    d0 = int(w.distribution[0])
+    return np.array([s < d0 and int(w.q_lens[s]) == 1 for s in range(w.num_seqs)])
+
+
+def algorithmic_work(w):
+    """Algorithmic HBM bytes and flops of the decode and prefill kernels.
+
+    bytes: every key/value inside the causal/window band read once (cache
+    rows 2*Hkv*D*elem per cached key; new tokens read from the bf16 inputs),
+    the new tokens' page write, the queries read and the outputs written.
+    flops: 4*D*Hq per unmasked (query token, key) pair."""
+    H, Hq, D, e = w.num_kv_heads, w.num_q_heads, w.head_dim, w.elem_bytes
+    W = w.sliding_window
+    dec = classify(w)
+    out = {"decode": {"bytes": 0, "flops": 0, "tokens": 0},
+           "prefill": {"bytes": 0, "flops": 0, "tokens": 0}}
+    for s in range(w.num_seqs):
+        q, kv = int(w.q_lens[s]), int(w.kv_lens_valid[s])
+        if q == 0:
+            continue
+        ctx = kv - q
+        first = ctx  # position of the first new token
+        lo_first = max(0, first - W + 1) if W else 0
+        cached_needed = max(0, ctx - lo_first)  # cached keys any token of the seq needs
+        pos = np.arange(ctx, kv, dtype=np.int64)
+        keys_per_tok = np.minimum(pos + 1, W) if W else pos + 1
+        k = out["decode" if dec[s] else "prefill"]
+        k["bytes"] += cached_needed * 2 * H * D * e + q * 2 * H * D * (2 + e) + 2 * q * Hq * D * 2
+        k["flops"] += int(keys_per_tok.sum()) * 4 * D * Hq
+        k["tokens"] += q
+    return out
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.path = tempfile.mktemp(prefix="rpa_clocks_", suffix=".csv")
+        self.proc = None
+        self.dev = device_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.4)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[3], parts[4:]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples under load: the upper half of the SM clock distribution
+        sm = [r[0] for r in rows]
+        reasons = set()
+        names = ("active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap")
+        for r in rows:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------------- peaks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def traffic_for(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel's
+    source is unchanged since the capture; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+        ent = table[workload]
+        src = os.path.join(ROOT, "ragged_paged_attention_kv_gb300", "csrc", ent["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != ent["source_sha"] or ent["source"] != kernel_file:
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------- GPU arm
+def setup_dist(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def gpu_arm(args, world, rank, local):
+    import ragged_paged_attention_kv_gb300 as rpa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.get(args.workload)
+    work = algorithmic_work(w)
+    fp8 = w.kv_dtype == "fp8"
+    q, k, v = w.make_qkv()
+    sink = w.make_sink()
+    meta_host = {"kv_lens": torch.from_numpy(w.kv_lens), "block_tables": torch.from_numpy(w.block_tables),
+                 "qsl": torch.from_numpy(w.query_start_loc), "dist": torch.from_numpy(w.distribution)}
+    dq, dk, dv = q.to(dev), k.to(dev), v.to(dev)
+    dsink = sink.to(dev) if sink is not None else None
+    dmeta = {n: t.to(dev) for n, t in meta_host.items()}
+    pool = w.make_pool(dev)
+    out = torch.empty_like(dq)
+    params = rpa.make_params(**w.params())
+    ws = rpa.alloc_workspace(params, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(softmax_scale=w.softmax_scale, sliding_window=w.sliding_window,
+              logits_soft_cap=w.logits_soft_cap, k_scale=w.k_scale if fp8 else None,
+              v_scale=w.v_scale if fp8 else None)
+
+    def step(events=None, src=None):
+        a = src or (dq, dk, dv, dmeta, dsink)
+        rpa.forward(a[0], a[1], a[2], pool, a[3]["kv_lens"], a[3]["block_tables"], a[3]["qsl"],
+                    a[3]["dist"], a[4], out=out, workspace=ws, events=events, **kw)
+
+    def new_events(n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        for e4 in evs:  # create the driver events before they are handed over
+            for e in e4:
+                e.record(stream)
+        return evs
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    if rpa.get_status(ws) != 0:
+        raise RuntimeError("device status nonzero after warm-up")
+
+    evs = new_events(args.steps)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        clocks.start()
+    barrier(world)
+    for i in range(args.steps):
+        flush.zero_()
+        step(events=evs[i])
+    barrier(world)
+    clk = clocks.stop() if rank == 0 else None
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    plan_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    pf_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+    ms_per_step = total_s * 1e3 / args.steps
+    tokens = w.num_query_tokens
+    value = tokens * world * args.steps / total_s
+
+    # ---- end to end through the public call, host buffers, copies inside the region
+    pin = lambda t: t.pin_memory() if t is not None else None
+    hq, hk, hv, hs = pin(q), pin(k), pin(v), pin(sink)
+    hmeta = {n: pin(t) for n, t in meta_host.items()}
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    eq, ek, ev = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+    es = torch.empty_like(dsink) if dsink is not None else None
+    emeta = {n: torch.empty_like(t) for n, t in dmeta.items()}
+    h2d = sum(t.numel() * t.element_size() for t in [hq, hk, hv, *hmeta.values()] + ([hs] if hs is not None else []))
+    d2h = hout.numel() * hout.element_size()
+    e2e_ms = []
+    barrier(world)
+    for i in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        eq.copy_(hq, non_blocking=True)
+        ek.copy_(hk, non_blocking=True)
+        ev.copy_(hv, non_blocking=True)
+        if es is not None:
+            es.copy_(hs, non_blocking=True)
+        for n in emeta:
+            emeta[n].copy_(hmeta[n], non_blocking=True)
+        step(src=(eq, ek, ev, emeta, es))
+        hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e0.synchronize()
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    barrier(world)
+    e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, world)
+    e2e_value = tokens * world * args.steps / e2e_s
+
+    # ---- roofline of the dominant kernel
+    peaks = load_peaks()
+    dec_avg, pf_avg = statistics.mean(dec_ms), statistics.mean(pf_ms)
+    if work["decode"]["tokens"] and dec_avg >= pf_avg:
+        kernel, kfile = "decode_kernel", "decode.cu"
+        achieved = work["decode"]["bytes"] / (dec_avg * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        kernel, kfile = "prefill_kernel", "prefill.cu"
+        achieved = work["prefill"]["flops"] / (pf_avg * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = traffic_for(kfile, args.workload)
+    roof["kernel"] = kernel
+    roof["peak_source"] = peaks["source"]
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "tokens_per_step": tokens, "l2": "flushed before every timed step "
+                   "(256 MB write, outside the events)", "parallelism": f"replicas x{world}",
+                   "kv_dtype": w.kv_dtype},
+        "roofline": roof,
+        "kernels_ms": {"plan": round(statistics.mean(plan_ms), 4),
+                       "decode": round(dec_avg, 4), "prefill": round(pf_avg, 4)},
+        "decode_kv_gbs": round(work["decode"]["bytes"] / (dec_avg * 1e-3) / 1e9, 1)
+        if work["decode"]["tokens"] else None,
+        "prefill_tflops": round(work["prefill"]["flops"] / (pf_avg * 1e-3) / 1e12, 2)
+        if work["prefill"]["tokens"] else None,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_s * 1e3 / args.steps, 4)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    return res, w
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(w, budget_s: float, seed: int = 0, nthreads: int = 0):
+    """Times the oracle on a seeded sample of the workload's sequences: the
+    page write plus the attention of every new token of each sampled
+    sequence (a seeded sample of rows for long prefills), adding sequences
+    until about budget_s of CPU time has been spent.  Returns (tokens/s,
+    threads used, description of the sample)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.num_seqs)
+    q_all, k_all, v_all = _qkv(w)
+    sink = w.make_sink()
+    done_tokens, spent, n_seqs = 0, 0.0, 0
+    rows_note = "all new tokens of each"
+    for s in order:
+        if spent >= budget_s:
+            break
+        s = int(s)
+        if int(w.q_lens[s]) == 0:
+            continue
+        sub, sub_pool, tmap = w.subset([s], None)
+        idx = torch.as_tensor(tmap)
+        q, k, v = q_all[idx], k_all[idx], v_all[idx]
+        p = oracle.make_params(**sub.params())
+        q_len = int(w.q_lens[s])
+        keys = min(int(w.kv_lens_valid[s]), w.sliding_window) if w.sliding_window else int(w.kv_lens_valid[s])
+        rows = np.arange(q_len)
+        if q_len * keys > 4_000_000:  # long prefill: a seeded sample of its rows
+            n = max(1, 4_000_000 // max(1, keys))
+            rows = np.unique(rng.integers(0, q_len, size=n))
+            rows_note = "all new tokens of each (a seeded row sample for long prefills)"
+        cache = sub_pool.contiguous().view(torch.uint8).numpy().reshape(-1).copy()
+        t0 = time.perf_counter()
+        cache = oracle.update_cache(p, k, v, cache, sub.kv_lens, sub.block_tables,
+                                    sub.query_start_loc, sub.num_seqs)
+        oracle.attention_rows(p, q, cache, sub.kv_lens, sub.block_tables, sub.query_start_loc,
+                              sub.num_seqs, rows, None if sink is None else sink.numpy(), nthreads)
+        spent += time.perf_counter() - t0
+        done_tokens += len(rows)
+        n_seqs += 1
+    value = done_tokens / spent if spent > 0 else 0.0
+    desc = (f"{n_seqs} of {w.num_seqs} sequences (seeded order), {rows_note}: "
+            f"{done_tokens} tokens in {spent:.1f} s")
+    return value, oracle.max_threads(), desc
+
+
+_QKV_CACHE = {}
+
+
+def _qkv(w):
+    if w.name not in _QKV_CACHE:
+        _QKV_CACHE[w.name] = w.make_qkv()
+    return _QKV_CACHE[w.name]
+
+
+def reference_arm(args, world, rank):
+    """The oracle as the reference arm: each step is a bounded sample."""
+    if rank != 0:
+        return None
+    w = wl.get(args.workload)
+    per_step = max(0.2, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step, seed=0)
+    vals = []
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        val, cores, desc = oracle_sample(w, per_step, seed=1 + i)
+        vals.append(val)
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(wall * 1e3 / max(1, args.steps), 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": f"per step ~{per_step:.1f} s: {desc}"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        res = reference_arm(args, world, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+
+    world, rank, local = setup_dist(args)
+    if world != args.gpus and rank == 0:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    res, w = gpu_arm(args, world, rank, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            val, cores, desc = oracle_sample(w, args.cpu_budget)
+            res["cpu_baseline"] = {"value": round(val, 3), "unit": "tokens/s", "cores": cores,
+                                   "kind": "oracle", "sample": desc}
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,193 @@
+// Shared device helpers for the ragged paged attention kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rpa.h"
+
+namespace rpa {
+
+// ------------------------------------------------------------------ layout
+// Workspace: a 256-byte header of int32 words, then the arrays below at
+// offsets computed by WorkspaceLayout (host and device agree through it).
+enum HeaderWord {
+  kHdrStatus = 0,       // RPA_STATUS_* bits, cleared by the planner
+  kHdrNumDecode = 1,    // decode work units planned
+  kHdrNumPrefill = 2,   // prefill work units planned
+  kHdrDecodeChunk = 3,  // keys per decode split
+  kHdrDecodeNext = 4,   // dynamic scheduler counter (decode)
+  kHdrPrefillNext = 5,  // dynamic scheduler counter (prefill)
+  kHdrWords = 64,
+};
+
+// Decode unit: one (sequence, kv head, key split).
+struct DecodeUnit {
+  int32_t seq, head, k_begin, k_end;    // keys [k_begin, k_end) of this split
+  int32_t split, nsplit, first_unit, pad;  // units of one (seq, head) are contiguous
+};
+
+// Prefill unit: one (sequence, tile of new tokens, kv head).
+struct PrefillUnit {
+  int32_t seq, t_begin, t_end, head;    // new tokens [t_begin, t_end) of seq
+};
+
+constexpr int kDecodeUnitsTarget = 4096;  // planner aims for about this many splits
+constexpr int kDecodeChunkMin = 256;      // smallest split, in keys
+constexpr int kDecodeRows = 16;           // q-heads per decode tile (padded group)
+constexpr int kPrefillRows = 64;          // packed (token, q-head) rows per prefill tile
+
+struct WorkspaceLayout {
+  size_t decode_units_off, counters_off, partial_o_off, partial_ml_off, prefill_units_off;
+  size_t total;
+  int64_t max_decode_units, max_prefill_units;
+
+  __host__ __device__ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+  __host__ __device__ explicit WorkspaceLayout(const rpa_params_t& p) {
+    const int64_t g = p.num_q_heads / p.num_kv_heads;
+    max_decode_units = (int64_t)kDecodeUnitsTarget + (int64_t)p.max_num_seqs * p.num_kv_heads;
+    const int64_t tiles = ((int64_t)p.total_tokens * g + kPrefillRows - 1) / kPrefillRows +
+                          p.max_num_seqs;
+    max_prefill_units = tiles * p.num_kv_heads;
+    size_t off = kHdrWords * sizeof(int32_t);
+    decode_units_off = off;
+    off = align_up(off + max_decode_units * sizeof(DecodeUnit), 256);
+    counters_off = off;
+    off = align_up(off + (size_t)p.max_num_seqs * p.num_kv_heads * sizeof(int32_t), 256);
+    partial_o_off = off;
+    off = align_up(off + (size_t)max_decode_units * g * p.head_dim * sizeof(float), 256);
+    partial_ml_off = off;
+    off = align_up(off + (size_t)max_decode_units * g * 2 * sizeof(float), 256);
+    prefill_units_off = off;
+    off = align_up(off + (size_t)max_prefill_units * sizeof(PrefillUnit), 256);
+    total = off;
+  }
+};
+
+// ----------------------------------------------------------------- status
+__device__ __forceinline__ void set_status(int32_t* ws_header, int bits) {
+  atomicOr(ws_header + kHdrStatus, bits);
+}
+
+// ---------------------------------------------------------- memory (PTX)
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                                  uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of 16-byte chunk `c` of row `r` in a tile whose rows are
+// `row_bytes` long: chunks are XOR-swizzled by the row's low 3 bits so that
+// eight consecutive rows at one logical chunk hit eight different banks.
+__device__ __forceinline__ uint32_t swz(int r, int c, int row_bytes) {
+  return (uint32_t)(r * row_bytes + ((c ^ (r & 7)) << 4));
+}
+
+// -------------------------------------------------------------- fp8 e4m3
+// Quantise two fp32 values (x / scale already applied) to e4m3 with round to
+// nearest even and saturation to +-448; x0 lands in the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float x0, float x1) {
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Two e4m3 codes (low byte first) -> two bf16 (exact), packed low-first.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+  float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+  return pack_bf16(f.x, f.y);
+}
+
+// Quantise 8 bf16 values (one 16-byte chunk) to 8 e4m3 codes: x / scale in
+// fp32 with an IEEE divide, then e4m3.  Returns the 8 codes as a uint2.
+__device__ __forceinline__ uint2 quantize8(uint4 src, float scale) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&src);
+  uint32_t w[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    float2 a = __bfloat1622float2(b[2 * i]);
+    float2 c = __bfloat1622float2(b[2 * i + 1]);
+    uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale));
+    uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(c.x, scale), __fdiv_rn(c.y, scale));
+    w[i] = lo | (hi << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+// 8 e4m3 codes -> 8 bf16 values (one 16-byte chunk).
+__device__ __forceinline__ uint4 dequant8(uint2 codes) {
+  uint4 r;
+  r.x = e4m3x2_to_bf16x2((uint16_t)(codes.x & 0xFFFF));
+  r.y = e4m3x2_to_bf16x2((uint16_t)(codes.x >> 16));
+  r.z = e4m3x2_to_bf16x2((uint16_t)(codes.y & 0xFFFF));
+  r.w = e4m3x2_to_bf16x2((uint16_t)(codes.y >> 16));
+  return r;
+}
+
+// ------------------------------------------------------------- reductions
+__device__ __forceinline__ float quad_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+  return x;
+}
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  return x;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Logit transform shared by the kernels: raw dot product -> log2-domain
+// logit.  scale_log2 = softmax_scale * k_scale * log2(e); with a soft cap,
+// cap * tanh(x / cap) is applied to the natural-domain logit first.
+struct LogitXform {
+  float scale_nat;   // softmax_scale * k_scale
+  float cap;         // 0 = none
+  float inv_cap;
+  float scale_log2;  // scale_nat * log2e (no cap)
+  __device__ __forceinline__ float operator()(float dot) const {
+    if (cap > 0.f) return cap * tanhf(dot * scale_nat * inv_cap) * kLog2e;
+    return dot * scale_log2;
+  }
+};
+
+}  // namespace rpa

@@ -1,0 +1,72 @@
+// New-KV page write shared by the standalone cache update and the fused
+// attention kernels (tpu-inference RPA v3 kernel.py, _update_kv_cache: the
+// step's keys/values land at positions ctx .. kv_len-1 of their sequence).
+#pragma once
+
+#include "common.cuh"
+
+namespace rpa {
+
+struct KvArgs {
+  rpa_params_t p;
+  const __nv_bfloat16* keys;    // [T, Hkv, D]
+  const __nv_bfloat16* values;  // [T, Hkv, D]
+  uint8_t* cache;               // [num_pages, P, 2*Hkv, D] (bf16 or e4m3 bytes)
+  const int32_t* block_tables;  // [max_num_seqs * pages_per_seq]
+  int32_t* ws;                  // workspace header
+};
+
+// Physical page of logical position `pos` of sequence `seq`, or -1 (and the
+// BAD_PAGE status bit) if the table entry lies outside the pool.
+__device__ __forceinline__ int32_t lookup_page(const KvArgs& a, int seq, int pos) {
+  const int32_t page =
+      __ldg(a.block_tables + (int64_t)seq * a.p.pages_per_seq + (pos / a.p.page_size));
+  if (page < 0 || page >= a.p.num_pages) {
+    set_status(a.ws, RPA_STATUS_BAD_PAGE);
+    return -1;
+  }
+  return page;
+}
+
+// Byte offset of (page, row, channel) in the pool.
+__device__ __forceinline__ int64_t pool_offset(const rpa_params_t& p, int64_t page, int row,
+                                               int channel, int elem_bytes) {
+  return ((page * p.page_size + row) * (2 * (int64_t)p.num_kv_heads) + channel) *
+         (int64_t)p.head_dim * elem_bytes;
+}
+
+// One warp writes key and value head `h` of input token `t` (sequence `seq`,
+// position `pos`) into the pool: a bf16 copy or fp8 quantisation x / scale.
+template <bool FP8>
+__device__ __forceinline__ void write_token_kv(const KvArgs& a, int seq, int t, int pos, int h,
+                                               int lane) {
+  const int D = a.p.head_dim;
+  const int chunks = D / 8;  // 16-byte chunks of one bf16 input row
+  const int32_t page = lookup_page(a, seq, pos);
+  if (page < 0) return;
+  const int64_t src = ((int64_t)t * a.p.num_kv_heads + h) * D;
+  const int64_t dst = pool_offset(a.p, page, pos % a.p.page_size, 2 * h, FP8 ? 1 : 2);
+  for (int i = lane; i < 2 * chunks; i += 32) {
+    const int kv = i / chunks, c = i % chunks;
+    const __nv_bfloat16* in = (kv ? a.values : a.keys) + src + c * 8;
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(in));
+    if (FP8) {
+      const float scale = kv ? a.p.v_scale : a.p.k_scale;
+      *reinterpret_cast<uint2*>(a.cache + dst + (int64_t)kv * D + c * 8) = quantize8(x, scale);
+    } else {
+      *reinterpret_cast<uint4*>(a.cache + dst + ((int64_t)kv * D + c * 8) * 2) = x;
+    }
+  }
+}
+
+// Arguments of the attention kernels.
+struct AttnArgs {
+  KvArgs kv;
+  const __nv_bfloat16* queries;  // [T, Hq, D]
+  const int32_t* kv_lens;        // [max_num_seqs]
+  const int32_t* qsl;            // [max_num_seqs + 1]
+  const float* sink;             // [Hq] or null
+  __nv_bfloat16* out;            // [T, Hq, D]
+};
+
+}  // namespace rpa

@@ -1,0 +1,233 @@
+// Planner and standalone page write.
+//
+// The planner reads the ragged metadata on the device (no host round trip),
+// checks it, and splits the batch into work units by class: sequences of the
+// decode-only class (distribution[0]) become (sequence, kv head, key split)
+// units with one new token each; the chunked-prefill and mixed classes become
+// (sequence, tile of new tokens, kv head) units.  The ejkernel
+// ragged_page_attention_v3 interface's `distribution` argument defines the
+// classes; results never depend on it (a decode-class sequence with
+// q_len != 1 is flagged and planned as a prefill).
+#include "common.cuh"
+#include "kv_write.cuh"
+
+namespace rpa {
+
+constexpr int kPlanThreads = 1024;
+
+// Block-wide exclusive scan of one int per thread; returns the prefix and
+// writes the block total to *total.  All threads of the block must call it.
+__device__ int block_exclusive_scan(int v, int* total, int* smem /* 33 ints */) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) smem[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (int)(blockDim.x >> 5) ? smem[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    smem[lane] = w;  // inclusive prefix over warps
+    if (lane == 31) smem[32] = w;
+  }
+  __syncthreads();
+  const int excl = x - v + (warp > 0 ? smem[warp - 1] : 0);
+  *total = smem[32];
+  __syncthreads();
+  return excl;
+}
+
+struct SeqPlan {
+  int cls;        // 0 none, 1 decode, 2 prefill
+  int q0, q_len, kv_len, lo;
+  int flags;      // RPA_STATUS_* bits raised by this sequence
+};
+
+__device__ SeqPlan classify(const rpa_params_t& p, int s, int d0, const int32_t* kv_lens,
+                            const int32_t* qsl) {
+  SeqPlan sp{0, 0, 0, 0, 0, 0};
+  const int a = qsl[s], b = qsl[s + 1];
+  const int kv = kv_lens[s];
+  if (a < 0 || b < a || b > p.total_tokens) {
+    sp.flags = RPA_STATUS_BAD_QUERY_START_LOC;
+    return sp;
+  }
+  const int q_len = b - a;
+  if (kv < q_len || (int64_t)kv > (int64_t)p.pages_per_seq * p.page_size) {
+    sp.flags = RPA_STATUS_BAD_KV_LEN;
+    return sp;
+  }
+  sp.q0 = a;
+  sp.q_len = q_len;
+  sp.kv_len = kv;
+  if (q_len == 0) return sp;
+  bool decode = s < d0;
+  if (decode && q_len != 1) {
+    sp.flags = RPA_STATUS_DECODE_QLEN;
+    decode = false;
+  }
+  sp.cls = decode ? 1 : 2;
+  sp.lo = (p.sliding_window > 0 && kv - p.sliding_window > 0) ? kv - p.sliding_window : 0;
+  return sp;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, const int32_t* kv_lens,
+                                                            const int32_t* qsl,
+                                                            const int32_t* dist, int32_t* ws) {
+  __shared__ int s_flags;
+  __shared__ int s_scan[33];
+  __shared__ unsigned long long s_keys;
+  const WorkspaceLayout L(p);
+  DecodeUnit* dunits = reinterpret_cast<DecodeUnit*>(reinterpret_cast<char*>(ws) + L.decode_units_off);
+  PrefillUnit* punits =
+      reinterpret_cast<PrefillUnit*>(reinterpret_cast<char*>(ws) + L.prefill_units_off);
+  int32_t* counters = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + L.counters_off);
+  const int tid = threadIdx.x;
+  const int Hkv = p.num_kv_heads, G = p.num_q_heads / p.num_kv_heads;
+  const int tile_tokens = kPrefillRows / G;
+
+  if (tid == 0) {
+    s_flags = 0;
+    s_keys = 0ull;
+  }
+  __syncthreads();
+  const int d0 = dist[0], d1 = dist[1], d2 = dist[2];
+  int S = d2;
+  if (!(0 <= d0 && d0 <= d1 && d1 <= d2 && d2 <= p.max_num_seqs)) {
+    if (tid == 0) atomicOr(&s_flags, RPA_STATUS_BAD_DISTRIBUTION);
+    S = 0;
+  }
+  if (tid == 0 && S > 0 && qsl[0] != 0) atomicOr(&s_flags, RPA_STATUS_BAD_QUERY_START_LOC);
+
+  // Pass 1: total decode keys (per kv head) to size the splits.
+  unsigned long long my_keys = 0;
+  for (int s = tid; s < S; s += kPlanThreads) {
+    SeqPlan sp = classify(p, s, d0, kv_lens, qsl);
+    if (sp.flags) atomicOr(&s_flags, sp.flags);
+    if (sp.cls == 1) my_keys += (unsigned long long)(sp.kv_len - sp.lo);
+  }
+  atomicAdd(&s_keys, my_keys);
+  __syncthreads();
+  const unsigned long long want =
+      (s_keys * (unsigned long long)Hkv + kDecodeUnitsTarget - 1) / kDecodeUnitsTarget;
+  int chunk = (int)((want + 15) / 16 * 16);
+  if (chunk < kDecodeChunkMin) chunk = kDecodeChunkMin;
+
+  // Pass 2: emit units in sequence order (prefill tiles last-first, so the
+  // longest causal tiles start first under the dynamic scheduler).
+  int dec_base = 0, pf_base = 0;
+  for (int base = 0; base < S; base += kPlanThreads) {
+    const int s = base + tid;
+    SeqPlan sp{0, 0, 0, 0, 0, 0};
+    int nsplit = 0, ntiles = 0;
+    if (s < S) {
+      sp = classify(p, s, d0, kv_lens, qsl);  // flags were taken in pass 1
+      if (sp.cls == 1) nsplit = (sp.kv_len - sp.lo + chunk - 1) / chunk;
+      if (sp.cls == 2) ntiles = (sp.q_len + tile_tokens - 1) / tile_tokens;
+    }
+    int dec_total, pf_total;
+    const int dec_off = dec_base + block_exclusive_scan(nsplit * Hkv, &dec_total, s_scan);
+    const int pf_off = pf_base + block_exclusive_scan(ntiles * Hkv, &pf_total, s_scan);
+    if (sp.cls == 1) {
+      for (int h = 0; h < Hkv; ++h) {
+        counters[(int64_t)s * Hkv + h] = 0;
+        const int first = dec_off + h * nsplit;
+        for (int k = 0; k < nsplit; ++k) {
+          DecodeUnit u;
+          u.seq = s;
+          u.head = h;
+          u.k_begin = sp.lo + k * chunk;
+          u.k_end = min(sp.kv_len, sp.lo + (k + 1) * chunk);
+          u.split = k;
+          u.nsplit = nsplit;
+          u.first_unit = first;
+          u.pad = 0;
+          dunits[first + k] = u;
+        }
+      }
+    } else if (sp.cls == 2) {
+      for (int r = 0; r < ntiles; ++r) {
+        const int t = ntiles - 1 - r;
+        for (int h = 0; h < Hkv; ++h) {
+          PrefillUnit u;
+          u.seq = s;
+          u.t_begin = t * tile_tokens;
+          u.t_end = min(sp.q_len, (t + 1) * tile_tokens);
+          u.head = h;
+          punits[pf_off + r * Hkv + h] = u;
+        }
+      }
+    }
+    dec_base += dec_total;
+    pf_base += pf_total;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    ws[kHdrStatus] = s_flags;
+    ws[kHdrNumDecode] = dec_base;
+    ws[kHdrNumPrefill] = pf_base;
+    ws[kHdrDecodeChunk] = chunk;
+    ws[kHdrDecodeNext] = 0;
+    ws[kHdrPrefillNext] = 0;
+  }
+}
+
+// Standalone page write: one warp per (token, kv head) of every planned unit.
+template <bool FP8>
+__global__ void __launch_bounds__(256) cache_write_kernel(KvArgs a, const int32_t* kv_lens,
+                                                          const int32_t* qsl) {
+  const WorkspaceLayout L(a.p);
+  const DecodeUnit* dunits =
+      reinterpret_cast<const DecodeUnit*>(reinterpret_cast<const char*>(a.ws) + L.decode_units_off);
+  const PrefillUnit* punits =
+      reinterpret_cast<const PrefillUnit*>(reinterpret_cast<const char*>(a.ws) + L.prefill_units_off);
+  const int n_dec = a.ws[kHdrNumDecode], n_pf = a.ws[kHdrNumPrefill];
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  // decode units: split 0 of each (seq, head) writes the single new token
+  for (int u = gw; u < n_dec; u += warps) {
+    const DecodeUnit d = dunits[u];
+    if (d.split != 0) continue;
+    const int t = qsl[d.seq];
+    write_token_kv<FP8>(a, d.seq, t, kv_lens[d.seq] - 1, d.head, lane);
+  }
+  // prefill units: every token of the tile for the unit's head
+  const int tile_tokens = kPrefillRows / (a.p.num_q_heads / a.p.num_kv_heads);
+  const int64_t n_items = (int64_t)n_pf * tile_tokens;
+  for (int64_t it = gw; it < n_items; it += warps) {
+    const PrefillUnit pu = punits[it / tile_tokens];
+    const int i = pu.t_begin + (int)(it % tile_tokens);
+    if (i >= pu.t_end) continue;
+    const int q0 = qsl[pu.seq];
+    const int q_len = qsl[pu.seq + 1] - q0;
+    const int ctx = kv_lens[pu.seq] - q_len;
+    write_token_kv<FP8>(a, pu.seq, q0 + i, ctx + i, pu.head, lane);
+  }
+}
+
+// ------------------------------------------------------------ host launch
+cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int32_t* qsl,
+                        const int32_t* dist, int32_t* ws, cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, kv_lens, qsl, dist, ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cache_write(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,
+                               int num_sms, cudaStream_t stream) {
+  const int grid = num_sms * 4;
+  if (a.p.kv_dtype == RPA_KV_FP8_E4M3)
+    cache_write_kernel<true><<<grid, 256, 0, stream>>>(a, kv_lens, qsl);
+  else
+    cache_write_kernel<false><<<grid, 256, 0, stream>>>(a, kv_lens, qsl);
+  return cudaGetLastError();
+}
+
+}  // namespace rpa

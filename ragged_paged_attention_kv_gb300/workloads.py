@@ -163,15 +163,17 @@ class Workload:
         return pool
 
     # -------------------------------------------------------------- subsets
-    def subset(self, seq_ids: Sequence[int], pool_before: torch.Tensor,
+    def subset(self, seq_ids: Sequence[int], pool_before: Optional[torch.Tensor],
                slack_pages: int = 2):
         """A compact copy of the listed sequences for CPU checks.
 
         Returns (sub_workload, sub_pool_cpu, token_map) where the sub-workload
         keeps the same options, its pool holds only the pages those sequences
-        use (copied from ``pool_before``, plus ``slack_pages`` seeded spare
-        pages) with the block tables renumbered, and token_map[i] is the row
-        of the full batch that sub-batch row i came from."""
+        use (copied from ``pool_before``, plus ``slack_pages`` spare pages)
+        with the block tables renumbered, and token_map[i] is the row of the
+        full batch that sub-batch row i came from.  With pool_before=None the
+        compact pool is filled with fresh seeded data instead (for timing runs
+        that never compare values)."""
         seq_ids = [int(s) for s in seq_ids]
         pages = [self.pages_of(s) for s in seq_ids]
         n_used = int(sum(len(p) for p in pages))
@@ -183,12 +185,17 @@ class Workload:
         for i, p in enumerate(pages):
             bt[i * pps: i * pps + len(p)] = np.arange(c, c + len(p))
             c += len(p)
-        idx = torch.as_tensor(src, device=pool_before.device)
-        sub_pool = torch.empty((n_pool,) + tuple(pool_before.shape[1:]), dtype=pool_before.dtype)
-        if n_used:
-            sub_pool[:n_used] = pool_before.index_select(0, idx).cpu()
-        if slack_pages:
-            sub_pool[n_used:] = pool_before[:slack_pages].cpu()
+        if pool_before is None:
+            tmp = dataclasses.replace(self, num_pages=n_pool)
+            sub_pool = tmp.make_pool("cpu")
+        else:
+            idx = torch.as_tensor(src, device=pool_before.device)
+            sub_pool = torch.empty((n_pool,) + tuple(pool_before.shape[1:]),
+                                   dtype=pool_before.dtype)
+            if n_used:
+                sub_pool[:n_used] = pool_before.index_select(0, idx).cpu()
+            if slack_pages:
+                sub_pool[n_used:] = pool_before[:slack_pages].cpu()
         qsl = self.query_start_loc
         token_map = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in seq_ids]).astype(np.int64) \
             if seq_ids else np.zeros(0, np.int64)
@@ -295,6 +302,27 @@ def decode() -> Workload:
                     distribution=np.array([S, S, S], np.int32), total_tokens=S)
 
 
+def decode_small() -> Workload:
+    """The decode workload's shape and length mix at a quarter of the batch
+    (64 sequences) with a pool of the pages used + 10%: small enough for a
+    many-pass profiler capture, still far above L2."""
+    seed = 1012
+    g = torch.Generator().manual_seed(seed)
+    S, P = 64, 16
+    kv = _randint(g, 512, 4096, S)
+    q = np.ones(S, np.int32)
+    pps = 4096 // P
+    need = int(sum(-(-int(k) // P) for k in kv))
+    num_pages = int(math.ceil(need * 1.1))
+    bt = _assign_pages(kv, P, num_pages, S, pps, g)
+    return Workload(name="decode_small", seed=seed, num_q_heads=32, num_kv_heads=8,
+                    head_dim=128, page_size=P, num_pages=num_pages, pages_per_seq=pps,
+                    max_num_seqs=S, kv_dtype="bf16", softmax_scale=1.0 / math.sqrt(128),
+                    sliding_window=0, logits_soft_cap=0.0, k_scale=1.0, v_scale=1.0,
+                    has_sink=False, q_lens=q, kv_lens_valid=kv, block_tables=bt,
+                    distribution=np.array([S, S, S], np.int32), total_tokens=S)
+
+
 def mixed() -> Workload:
     seed = 1003
     g = torch.Generator().manual_seed(seed)
@@ -358,6 +386,7 @@ def fp8() -> Workload:
 WORKLOADS = {
     "tiny": tiny,
     "decode": decode,
+    "decode_small": decode_small,
     "mixed": mixed,
     "long": lambda: long(0),
     "long_w4096": lambda: long(4096),

@@ -1,0 +1,107 @@
+"""The C ABI loads and behaves on the host (no GPU needed).
+
+Checks that librpa.so exports every function include/rpa.h declares, that
+workspace sizing works, and that host-checkable argument errors are refused
+before anything touches the GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ragged_paged_attention_kv_gb300 import _lib, build
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(rpa_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("rpa_forward", "rpa_update_cache", "rpa_workspace_size", "rpa_get_status",
+                 "rpa_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _params(**over):
+    from ragged_paged_attention_kv_gb300 import make_params
+    kw = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, num_pages=80000,
+              pages_per_seq=256, max_num_seqs=256, total_tokens=256)
+    kw.update(over)
+    return make_params(**kw)
+
+
+def test_workspace_size_host_only(lib):
+    from ragged_paged_attention_kv_gb300 import workspace_size
+    n = workspace_size(_params())
+    assert 0 < n < 1 << 30
+    assert workspace_size(_params(total_tokens=65536, max_num_seqs=2)) > 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(head_dim=96), 2),
+    (dict(num_q_heads=24, num_kv_heads=8), 2),
+    (dict(num_q_heads=30, num_kv_heads=8), 2),
+    (dict(page_size=24), 2),
+    (dict(num_pages=0), 1),
+    (dict(sliding_window=-1), 1),
+    (dict(k_scale=0.5), 1),              # bf16 cache needs unit scales
+    (dict(kv_fp8=True, k_scale=0.0), 1),
+    (dict(logits_soft_cap=-1.0), 1),
+])
+def test_invalid_params_are_refused(lib, over, code):
+    n = ctypes.c_size_t(0)
+    p = _params(**over)
+    assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == code
+    # rpa_forward refuses the same params before touching any pointer or the GPU
+    z = ctypes.c_void_p(16)
+    assert lib.rpa_forward(ctypes.byref(p), z, z, z, z, z, z, z, z, None, z, z, 1 << 40, None) == code
+
+
+def test_null_pointers_and_workspace_are_refused(lib):
+    p = _params()
+    z = ctypes.c_void_p(256)
+    assert lib.rpa_forward(ctypes.byref(p), None, z, z, z, z, z, z, z, None, z, z, 1 << 40, None) == 1
+    n = ctypes.c_size_t(0)
+    lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n))
+    # too small, misaligned, null
+    assert lib.rpa_forward(ctypes.byref(p), z, z, z, z, z, z, z, z, None, z, z, n.value - 1, None) == 3
+    assert lib.rpa_forward(ctypes.byref(p), z, z, z, z, z, z, z, z, None, z,
+                           ctypes.c_void_p(257), n.value, None) == 3
+    assert lib.rpa_forward(ctypes.byref(p), z, z, z, z, z, z, z, z, None, z, None, n.value, None) == 3
+    assert lib.rpa_update_cache(ctypes.byref(p), None, z, z, z, z, z, z, z, n.value, None) == 1
+    assert lib.rpa_get_status(None, None, None) == 1
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.rpa_status_string(code)
+    assert lib.rpa_status_string(99) == b"unknown code"
+
+
+def test_binding_raises_without_library(monkeypatch, tmp_path):
+    from ragged_paged_attention_kv_gb300 import _lib
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _lib.load()

@@ -1,0 +1,354 @@
+"""GPU parity: librpa.so against the CPU oracle (needs a GB300).
+
+Every case calls the C ABI (through the ctypes binding) on seeded inputs and
+compares with the oracle on the same inputs:
+  * the whole page pool after the call, bit for bit (new slots written, every
+    other byte untouched);
+  * the attention output, element by element: the error beyond half a bf16
+    ulp of the exact value (the rounding any bf16 output carries) is at most
+    1e-2, and the mean absolute difference from the fp64 oracle at most 1e-3.
+Small cases span several tiles, several decode splits and ragged tails;
+the full-size workloads are checked on sampled sequences/tokens in the
+launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ragged_paged_attention_kv_gb300 as rpa
+from helpers import assert_close, bf16_half_ulp, pool_bytes, run_oracle
+from ragged_paged_attention_kv_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _dev(x, dtype=None):
+    t = torch.as_tensor(x)
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(DEV).contiguous()
+
+
+def run_gpu(w, q, k, v, pool_before, sink=None, workspace=None, out=None):
+    """One rpa_forward on copies of the inputs; returns (out cpu, pool cpu, status)."""
+    pool = pool_before.to(DEV).clone()
+    out_t = out if out is not None else torch.full((w.total_tokens, w.num_q_heads, w.head_dim),
+                                                   7.0, dtype=torch.bfloat16, device=DEV)
+    params = rpa.make_params(**{k_: v_ for k_, v_ in w.params().items()
+                                if k_ not in ("kv_fp8",)}, kv_fp8=w.kv_dtype == "fp8")
+    ws = workspace if workspace is not None else rpa.alloc_workspace(params, DEV)
+    rpa.forward(_dev(q), _dev(k), _dev(v), pool, _dev(w.kv_lens), _dev(w.block_tables),
+                _dev(w.query_start_loc), _dev(w.distribution),
+                None if sink is None else _dev(sink),
+                softmax_scale=w.softmax_scale, sliding_window=w.sliding_window,
+                logits_soft_cap=w.logits_soft_cap,
+                k_scale=w.k_scale if w.kv_dtype == "fp8" else None,
+                v_scale=w.v_scale if w.kv_dtype == "fp8" else None, out=out_t, workspace=ws)
+    status = rpa.get_status(ws)
+    torch.cuda.synchronize()
+    return out_t.float().cpu().numpy().astype(np.float64), pool.cpu(), status
+
+
+def check_case(w, expect_status=0):
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu")
+    sink = w.make_sink()
+    ref_out, ref_cache = run_oracle(w, q, k, v, pool, sink)
+    out, pool_after, status = run_gpu(w, q, k, v, pool, sink)
+    assert status == expect_status, f"status {status:#x}"
+    assert np.array_equal(pool_bytes(pool_after), ref_cache), "page pool differs from the oracle"
+    n = w.num_query_tokens
+    assert_close(out[:n], ref_out, w.name)
+    # rows past query_start_loc[S] stay untouched
+    assert np.all(out[n:] == 7.0)
+    return out[:n], ref_out
+
+
+def _case(name, seed, q_lens, kv_lens, **kw):
+    base = dict(num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16)
+    base.update(kw)
+    return wl.make_custom(name, seed, q_lens, kv_lens, **base)
+
+
+def test_tiny_workload():
+    check_case(wl.tiny())
+
+
+CASES = [
+    # decode only, several splits per sequence (combine path), long and short
+    ("decode_splits", lambda: _case("ds", 101, [1] * 6, [700, 17, 1, 16, 33, 1290],
+                                    num_q_heads=32, num_kv_heads=8, head_dim=128)),
+    ("decode_g1_d64", lambda: _case("d1", 102, [1] * 5, [5, 64, 65, 300, 513],
+                                    num_q_heads=4, num_kv_heads=4)),
+    ("decode_g16", lambda: _case("d16", 103, [1] * 3, [100, 260, 31], num_q_heads=32,
+                                 num_kv_heads=2, head_dim=128, page_size=32)),
+    # prefill with many tiles and ragged tails, fresh and with context
+    ("prefill_fresh", lambda: _case("pf", 104, [150, 37], [150, 37], num_q_heads=16,
+                                    num_kv_heads=4, head_dim=128)),
+    ("prefill_chunk", lambda: _case("pc", 105, [70, 5, 129], [300, 260, 129], page_size=64)),
+    ("mixed_classes", lambda: _case("mx", 106, [1, 1, 1, 40, 9, 77], [90, 300, 2, 140, 9, 200],
+                                    num_q_heads=32, num_kv_heads=4, head_dim=128,
+                                    distribution=[3, 5, 6])),
+    ("q_len_zero", lambda: _case("qz", 107, [0, 3, 0, 1], [12, 30, 1, 7], distribution=[0, 0, 4])),
+    ("page_size_1", lambda: _case("p1", 108, [1, 6], [40, 20], page_size=1)),
+    ("page_size_256", lambda: _case("p256", 109, [1, 20], [600, 530], page_size=256)),
+    # options
+    ("window", lambda: _case("w", 110, [1, 1, 50, 100], [600, 20, 70, 300], sliding_window=37)),
+    ("window_pagealigned", lambda: _case("wp", 111, [1, 64], [512, 256], sliding_window=64,
+                                         head_dim=128)),
+    ("softcap", lambda: _case("sc", 112, [1, 33], [400, 120], logits_soft_cap=5.0,
+                              softmax_scale=0.6)),
+    ("sink", lambda: _case("sk", 113, [1, 1, 45], [333, 2, 45], has_sink=True)),
+    ("fp8", lambda: _case("f8", 114, [1, 1, 30, 8], [500, 3, 100, 8], kv_dtype="fp8",
+                          k_scale=0.05, v_scale=0.05)),
+    ("fp8_all_options", lambda: _case("f8a", 115, [1, 1, 1, 64, 20], [900, 129, 5, 200, 20],
+                                      kv_dtype="fp8", k_scale=0.05, v_scale=0.07, num_q_heads=64,
+                                      num_kv_heads=8, head_dim=64, logits_soft_cap=30.0,
+                                      has_sink=True, sliding_window=128, softmax_scale=0.125)),
+    ("fp8_d128", lambda: _case("f8d", 116, [1, 17], [260, 80], kv_dtype="fp8", k_scale=0.3,
+                               v_scale=0.1, head_dim=128)),
+    ("padding_rows", lambda: _case("pad", 117, [1, 5], [9, 12], max_num_seqs=5, extra_tokens=6,
+                                   pages_per_seq=4)),
+]
+
+
+@pytest.mark.parametrize("name,make", CASES, ids=[c[0] for c in CASES])
+def test_small_cases(name, make):
+    check_case(make())
+
+
+def test_decode_split_boundaries():
+    # kv lengths at page and split boundaries, all decode, big enough batch that
+    # the planner's split size stays at its minimum
+    kv = [255, 256, 257, 511, 512, 513, 16, 15, 17, 1024, 1025, 2048]
+    check_case(_case("db", 121, [1] * len(kv), kv, num_q_heads=16, num_kv_heads=4, head_dim=128))
+
+
+def test_distribution_only_selects_tiles():
+    # decode-class sequences go through the decode kernel, the others through
+    # the prefill kernel: the two tile shapes sum in different orders, so the
+    # results agree up to rounding, and each matches the oracle
+    w = _case("dist", 122, [1, 1, 12, 1], [40, 9, 30, 77])
+    outs = []
+    for dist in ([2, 2, 4], [0, 0, 4], [0, 2, 4]):
+        w.distribution = np.array(dist, np.int32)
+        out, ref = check_case(w)
+        outs.append(out)
+    for o in outs[1:]:
+        assert np.max(np.maximum(np.abs(o - outs[0]) - 2 * bf16_half_ulp(ref), 0)) <= 2e-2
+        assert np.mean(np.abs(o - outs[0])) <= 2e-3
+
+
+def test_decode_class_with_long_query_is_flagged_and_computed():
+    w = _case("dq", 123, [1, 3, 1], [30, 10, 5], distribution=[3, 3, 3])
+    check_case(w, expect_status=oracle_status_decode_qlen())
+
+
+def oracle_status_decode_qlen():
+    from ragged_paged_attention_kv_gb300 import _lib
+    return _lib.RPA_STATUS_DECODE_QLEN
+
+
+def test_repeat_calls_reuse_workspace():
+    w = _case("rep", 124, [1, 1, 20], [300, 1000, 50], num_q_heads=16, num_kv_heads=4)
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu")
+    params = rpa.make_params(**{a: b for a, b in w.params().items() if a != "kv_fp8"})
+    ws = rpa.alloc_workspace(params, DEV)
+    o1, p1, s1 = run_gpu(w, q, k, v, pool, workspace=ws)
+    o2, p2, s2 = run_gpu(w, q, k, v, pool, workspace=ws)
+    assert s1 == s2 == 0
+    assert np.array_equal(o1, o2) and torch.equal(p1, p2)
+
+
+# --------------------------------------------------------------- bad inputs
+def _status_of(w, mutate):
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu")
+    mutate(w)
+    out, pool_after, status = run_gpu(w, q, k, v, pool)
+    return status, out, pool, pool_after
+
+
+def test_bad_page_sets_status_without_fault():
+    from ragged_paged_attention_kv_gb300 import _lib
+    w = _case("bp", 131, [1, 4], [40, 30])
+
+    def mutate(w):
+        w.block_tables = w.block_tables.copy()
+        w.block_tables[0] = w.num_pages + 5    # decode seq, cached page
+        w.block_tables[w.pages_per_seq + 1] = -3  # prefill seq, page of its new tokens
+    status, _, _, _ = _status_of(w, mutate)
+    assert status & _lib.RPA_STATUS_BAD_PAGE
+
+
+def test_bad_kv_len_and_qsl_skip_sequence():
+    from ragged_paged_attention_kv_gb300 import _lib
+    w = _case("bk", 132, [1, 4, 3], [40, 30, 9])
+
+    def mutate(w):
+        w.kv_lens_valid = w.kv_lens_valid.copy()
+        w.kv_lens_valid[1] = 2  # < q_len
+    status, out, pool, pool_after = _status_of(w, mutate)
+    assert status == _lib.RPA_STATUS_BAD_KV_LEN
+    qsl = w.query_start_loc
+    assert np.all(out[qsl[1]:qsl[2]] == 7.0)  # the skipped sequence's rows untouched
+
+
+def test_bad_distribution_plans_nothing():
+    from ragged_paged_attention_kv_gb300 import _lib
+    w = _case("bd", 133, [1, 4], [40, 30])
+
+    def mutate(w):
+        w.distribution = np.array([2, 1, 2], np.int32)
+    status, out, pool, pool_after = _status_of(w, mutate)
+    assert status == _lib.RPA_STATUS_BAD_DISTRIBUTION
+    assert np.all(out == 7.0) and torch.equal(pool, pool_after)
+
+
+def test_host_errors_raise():
+    w = _case("he", 134, [1], [10])
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu").to(DEV)
+    with pytest.raises(rpa.RpaError):
+        rpa.forward(_dev(q), _dev(k), _dev(v), pool, _dev(w.kv_lens), _dev(w.block_tables),
+                    _dev(w.query_start_loc), _dev(w.distribution), k_scale=0.5)
+
+
+# ------------------------------------------------------------- update_cache
+@pytest.mark.parametrize("fp8", [False, True])
+def test_update_cache_alone_matches_oracle(fp8):
+    w = _case("uc", 141, [1, 1, 40, 3], [90, 1, 40, 300], kv_dtype="fp8" if fp8 else "bf16",
+              k_scale=0.05 if fp8 else 1.0, v_scale=0.2 if fp8 else 1.0)
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu")
+    p = oracle.make_params(**w.params())
+    ref = oracle.update_cache(p, k, v, pool_bytes(pool), w.kv_lens, w.block_tables,
+                              w.query_start_loc, w.num_seqs)
+    gpool = pool.to(DEV)
+    rpa.update_cache(_dev(k), _dev(v), gpool, _dev(w.kv_lens), _dev(w.block_tables),
+                     _dev(w.query_start_loc), _dev(w.distribution),
+                     k_scale=w.k_scale if fp8 else None, v_scale=w.v_scale if fp8 else None,
+                     num_q_heads=w.num_q_heads)
+    torch.cuda.synchronize()
+    assert np.array_equal(pool_bytes(gpool.cpu()), ref)
+
+
+def test_fp8_quantisation_sweep_matches_oracle():
+    """Every bf16 bit pattern in a wide range, quantised by the page write,
+    equals the oracle's E4M3 round-to-nearest-even with saturation."""
+    bits = np.arange(0, 1 << 16, dtype=np.uint32)
+    vals = bits.astype(np.uint16)
+    f = torch.from_numpy(vals.view(np.int16)).view(torch.bfloat16).float()
+    keep = torch.isfinite(f) & (f.abs() < 1e30)
+    vals = vals[keep.numpy()]
+    D, Hkv = 64, 1
+    n_tok = -(-len(vals) // (D * Hkv))
+    pad = n_tok * D - len(vals)
+    allv = np.concatenate([vals, np.zeros(pad, np.uint16)])
+    k = torch.from_numpy(allv.view(np.int16)).view(torch.bfloat16).view(n_tok, Hkv, D)
+    w = _case("sw", 142, [n_tok], [n_tok], num_q_heads=1, num_kv_heads=1, head_dim=D,
+              page_size=64, kv_dtype="fp8", k_scale=0.37, v_scale=1.0)
+    pool = w.make_pool("cpu")
+    gpool = pool.to(DEV)
+    rpa.update_cache(_dev(k), _dev(k), gpool, _dev(w.kv_lens), _dev(w.block_tables),
+                     _dev(w.query_start_loc), _dev(w.distribution), k_scale=0.37, v_scale=1.0,
+                     num_q_heads=1)
+    torch.cuda.synchronize()
+    p = oracle.make_params(**w.params())
+    ref = oracle.update_cache(p, k, k, pool_bytes(pool), w.kv_lens, w.block_tables,
+                              w.query_start_loc, w.num_seqs)
+    assert np.array_equal(pool_bytes(gpool.cpu()), ref)
+
+
+# ------------------------------------------------------- full-size workloads
+def _full_size(name, sample_seqs, sample_tokens_per_seq=None, nthreads=0):
+    """rpa_forward on the full workload, in the benchmark's launch
+    configuration; sampled sequences are checked against the oracle (outputs
+    and their pages) and the whole pool outside the new-token slots must be
+    unchanged."""
+    w = wl.get(name)
+    q, k, v = w.make_qkv()
+    sink = w.make_sink()
+    pool0 = w.make_pool(DEV)
+    pool = pool0.clone()
+    out = torch.full((w.total_tokens, w.num_q_heads, w.head_dim), 7.0, dtype=torch.bfloat16,
+                     device=DEV)
+    ws = rpa.alloc_workspace(rpa.make_params(**{a: b for a, b in w.params().items() if a != "kv_fp8"},
+                                             kv_fp8=w.kv_dtype == "fp8"), DEV)
+    fp8 = w.kv_dtype == "fp8"
+    rpa.forward(_dev(q), _dev(k), _dev(v), pool, _dev(w.kv_lens), _dev(w.block_tables),
+                _dev(w.query_start_loc), _dev(w.distribution), None if sink is None else _dev(sink),
+                softmax_scale=w.softmax_scale, sliding_window=w.sliding_window,
+                logits_soft_cap=w.logits_soft_cap, k_scale=w.k_scale if fp8 else None,
+                v_scale=w.v_scale if fp8 else None, out=out, workspace=ws)
+    assert rpa.get_status(ws) == 0
+    torch.cuda.synchronize()
+    # every new token's slot, and nothing else, changed as the page write says
+    qsl = w.query_start_loc
+    flat0 = pool0.view(w.num_pages * w.page_size, 2 * w.num_kv_heads, w.head_dim)
+    flat1 = pool.view(w.num_pages * w.page_size, 2 * w.num_kv_heads, w.head_dim)
+    slots = []
+    for s in range(w.num_seqs):
+        ctx = int(w.kv_lens_valid[s]) - int(w.q_lens[s])
+        pos = np.arange(ctx, int(w.kv_lens_valid[s]))
+        slots.append(w.block_tables[s * w.pages_per_seq + pos // w.page_size].astype(np.int64)
+                     * w.page_size + pos % w.page_size)
+    slots = torch.as_tensor(np.concatenate(slots), device=DEV)
+    changed = torch.zeros(flat0.shape[0], dtype=torch.bool, device=DEV)
+    changed[slots] = True
+    assert torch.equal(flat0[~changed], flat1[~changed])
+    kd, vd = k.to(DEV), v.to(DEV)
+    if fp8:
+        kd = (kd.float() / torch.tensor(np.float32(w.k_scale))).to(torch.float8_e4m3fn).view(torch.uint8)
+        vd = (vd.float() / torch.tensor(np.float32(w.v_scale))).to(torch.float8_e4m3fn).view(torch.uint8)
+    nq = w.num_query_tokens
+    assert torch.equal(flat1[slots][:, 0::2], kd[:nq]) and torch.equal(flat1[slots][:, 1::2], vd[:nq])
+    assert torch.all(out[nq:] == 7.0)
+    # sampled sequences against the oracle
+    sub, sub_pool, tmap = w.subset(sample_seqs, pool0)
+    p = oracle.make_params(**sub.params())
+    cache = oracle.update_cache(p, k[tmap], v[tmap], pool_bytes(sub_pool), sub.kv_lens,
+                                sub.block_tables, sub.query_start_loc, sub.num_seqs)
+    # the sampled pages after the call, bit for bit
+    pages = np.concatenate([w.pages_of(s) for s in sample_seqs]).astype(np.int64)
+    got_pages = pool.index_select(0, torch.as_tensor(pages, device=DEV)).cpu()
+    n_used = len(pages)
+    assert np.array_equal(pool_bytes(got_pages), cache[:n_used * (cache.size // sub.num_pages)])
+    if sample_tokens_per_seq is None:
+        rows = np.arange(len(tmap))
+    else:
+        rng = np.random.default_rng(5)
+        sqsl = sub.query_start_loc
+        rows = []
+        for i in range(sub.num_seqs):
+            a_, b_ = int(sqsl[i]), int(sqsl[i + 1])
+            pick = {a_, b_ - 1, a_ + (b_ - a_) // 2}
+            pick |= set(rng.integers(a_, b_, size=sample_tokens_per_seq).tolist())
+            rows += sorted(pick)
+        rows = np.array(rows)
+    ref = oracle.attention_rows(p, q[tmap], cache, sub.kv_lens, sub.block_tables,
+                                sub.query_start_loc, sub.num_seqs, rows,
+                                None if sink is None else sink.numpy(), nthreads)
+    got = out[torch.as_tensor(tmap[rows], device=DEV)].float().cpu().numpy().astype(np.float64)
+    assert_close(got, ref, name)
+
+
+def test_full_decode_workload():
+    _full_size("decode", sample_seqs=[0, 1, 77, 128, 255])
+
+
+def test_full_mixed_workload():
+    _full_size("mixed", sample_seqs=[0, 64, 127, 128, 133, 136, 137], sample_tokens_per_seq=6)
+
+
+def test_full_fp8_workload():
+    _full_size("fp8", sample_seqs=[0, 100, 511, 512, 519], sample_tokens_per_seq=8)
+
+
+@pytest.mark.parametrize("name", ["long", "long_w4096"])
+def test_full_long_workload(name):
+    _full_size(name, sample_seqs=[0, 1], sample_tokens_per_seq=6)
