@@ -148,6 +148,41 @@ int rpa_forward_timed(const rpa_params_t* params, const void* queries,
                       void* out, void* workspace, size_t workspace_bytes,
                       void* stream, void* const* events);
 
+/* rpa_forward for callers that cannot allocate device memory.  The pages
+ * describe no such call; it exists for code that has no way to obtain a
+ * workspace: a caller running inside a memory-pool or allocator callback
+ * (allocating there would re-enter the allocator), a plugin of a runtime that
+ * owns every device allocation, or a deployment that forbids allocation
+ * after start-up.
+ *
+ * Instead of a caller workspace it uses one fixed array of
+ * RPA_NOALLOC_WORKSPACE_BYTES in device global memory, reserved when the
+ * library is loaded and held by every GPU that loads it until the process
+ * exits.  The caller still passes all inputs and outputs, exactly as for
+ * rpa_forward, and gets the same results.  The call allocates nothing and
+ * calls no allocating routine.
+ *
+ * - Params whose workspace (rpa_workspace_size) exceeds the array are
+ *   refused with RPA_ERR_NOALLOC_TOO_LARGE; nothing is enqueued.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  Later calls reuse the address.
+ * - Every call on a device shares the one array and leaves its contents
+ *   behind; the planner rewrites every word the kernels read, so nothing has
+ *   to be cleared between calls.  Calls whose GPU work overlaps (on
+ *   different streams, or different host threads without ordering) race on
+ *   the array and give undefined results: serialise them.
+ * - The device status word of these calls is not readable through
+ *   rpa_get_status (there is no caller workspace to pass). */
+#define RPA_NOALLOC_WORKSPACE_BYTES (32u << 20)
+#define RPA_ERR_NOALLOC_TOO_LARGE 5
+int rpa_forward_noalloc(const rpa_params_t* params, const void* queries,
+                        const void* keys, const void* values, void* kv_cache,
+                        const int32_t* kv_lens, const int32_t* block_tables,
+                        const int32_t* query_start_loc,
+                        const int32_t* distribution,
+                        const float* attention_sink, void* out, void* stream);
+
 /* Copies the status word of the last call that used `workspace` on `stream`
  * to *device_status (a host int32) and synchronises the stream.  0 = clean. */
 int rpa_get_status(const void* workspace, void* stream, int32_t* device_status);

@@ -177,6 +177,8 @@ const char* rpa_status_string(int code) {
     case RPA_ERR_UNSUPPORTED: return "unsupported configuration";
     case RPA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case RPA_ERR_CUDA: return "CUDA runtime error";
+    case RPA_ERR_NOALLOC_TOO_LARGE:
+      return "params need more scratch than rpa_forward_noalloc's fixed device array";
     default: return "unknown code";
   }
 }
