@@ -29,6 +29,9 @@ static int check_params(const rpa_params_t* p) {
   if (p->head_dim != 64 && p->head_dim != 128) return RPA_ERR_UNSUPPORTED;
   if (!is_pow2(p->page_size) || p->page_size > 1024) return RPA_ERR_UNSUPPORTED;
   if (p->kv_dtype != RPA_KV_BF16 && p->kv_dtype != RPA_KV_FP8_E4M3) return RPA_ERR_UNSUPPORTED;
+  // fp8 rows of 64 bytes need at least two rows per page for 128-byte aligned copies
+  if (p->kv_dtype == RPA_KV_FP8_E4M3 && p->head_dim == 64 && p->page_size < 2)
+    return RPA_ERR_UNSUPPORTED;
   if (!(p->softmax_scale == p->softmax_scale) || !(p->logits_soft_cap >= 0.f))
     return RPA_ERR_INVALID_ARG;
   if (p->kv_dtype == RPA_KV_FP8_E4M3) {

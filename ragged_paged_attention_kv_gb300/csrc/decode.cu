@@ -1,99 +1,88 @@
 // Decode path: one new token per sequence, HBM-bound.
 //
 // Work unit = (sequence, kv head, split of the key range).  The q-heads of the
-// kv head (the GQA group, tpu-inference RPA v3 kernel.py stacks them as rows
+// kv head (the GQA group; tpu-inference RPA v3 kernel.py stacks them as rows
 // of one q block) form a 16-row tile, so every key/value byte fetched from a
-// page feeds all of them through one tensor-core MMA.  Keys/values stream
-// page by page from the pool into shared memory with 16-byte cp.async
-// (3-stage pipeline of 64 keys); the new token's key/value is taken from the
-// step's inputs, not from the cache (RPA v3 _fetch_bkv does the same), and
-// split 0 of each (sequence, kv head) writes it into its page.  Each warp
-// keeps an online-softmax state over its quarter of every stage (running max
-// m, sum l, accumulator O as in RPA v3 flash_attention_step1_qk_softmax /
-// step2_pv); the four warps merge in shared memory, and when a sequence's
+// page feeds all of them through one tensor-core MMA.
+//
+// The kernel is persistent and warp-specialised.  One producer warp walks the
+// planner's unit list (dynamic atomic counter) and streams each unit's pages
+// into a ring of shared-memory stages with TMA: per page, one 128-byte
+// swizzled box per (key | value, 64-wide half of head_dim), so consecutive
+// keys of one head land in consecutive conflict-free rows.  The query rows
+// arrive with a bulk copy.  Four consumer warps each take 16 keys of every
+// stage: S = Q K^T and O += P V with mma.sync, an online softmax in fp32
+// (RPA v3 flash_attention_step1_qk_softmax / step2_pv) whose running max is
+// only moved -- and O only rescaled -- when it grows by more than 2^8.
+//
+// The new token's key/value is taken from the step's inputs, not from its
+// page (RPA v3 _fetch_bkv reads new keys from the inputs too), and split 0
+// of each (sequence, kv head) writes it into the page.  When a sequence's
 // keys are split over several units, the unit that finishes last merges the
 // partial (m, l, O) of all splits with a log-sum-exp combine.
+#include "async.cuh"
 #include "common.cuh"
 #include "kv_write.cuh"
+#include "tma_host.h"
 
 namespace rpa {
-
 namespace dec {
 
-constexpr int kThreads = 128;
-constexpr int kWarps = 4;
-constexpr int kBN = 64;       // keys per stage
-constexpr int kStages = 3;
-constexpr int kKeysPerWarp = kBN / kWarps;  // 16
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kBN = 64;                       // keys per stage
+constexpr int kKeysPerWarp = kBN / kConsumerWarps;  // 16
+constexpr int kRescaleLog2 = 8;               // lazy-rescale threshold (log2 units)
 
 template <int D, bool FP8>
-struct Smem {
-  static constexpr int kElem = FP8 ? 1 : 2;
-  static constexpr int kRowBytes = D * kElem;          // one key (or value) row in the stage
-  static constexpr int kStageBytes = 2 * kBN * kRowBytes;
-  static constexpr int kQBytes = kDecodeRows * D * 2;
-  static constexpr int kConvBytes = FP8 ? kWarps * 2 * kKeysPerWarp * D * 2 : 0;
-  static constexpr int kMergeBytes = kWarps * kDecodeRows * (D + 2) * 4;
-  static constexpr int kStagesBytes = kStages * kStageBytes;
-  static constexpr int kLoopBytes = kStagesBytes + kConvBytes;
-  static constexpr int kBytes =
-      kQBytes + (kLoopBytes > kMergeBytes ? kLoopBytes : kMergeBytes);
+struct Cfg {
+  static constexpr int kRowBytes = FP8 ? D : 128;        // bytes of one box row in smem
+  static constexpr int kHalves = FP8 ? 1 : D / 64;       // boxes across head_dim
+  static constexpr int kHalfBytes = kBN * kRowBytes;
+  static constexpr int kKVBytes = kHalves * kHalfBytes;  // keys (or values) of one stage
+  static constexpr int kStageBytes = 2 * kKVBytes;
+  static constexpr int kQBytes = kDecodeRows * D * 2;    // one query slot
+  static constexpr int kConvBytes = FP8 ? kConsumerWarps * 2 * kKeysPerWarp * D * 2 : 0;
+  static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * (D + 2) * 4;
+  // as many stages as fit next to the other buffers (at most 12, 160 KB)
+  static constexpr int kBudget = 220 * 1024 - 2 * kQBytes - kConvBytes - kMergeBytes - 1024 - 256;
+  static constexpr int kStages1 = (kBudget < 160 * 1024 ? kBudget : 160 * 1024) / kStageBytes;
+  static constexpr int kStages = kStages1 > 12 ? 12 : (kStages1 < 2 ? 2 : kStages1);
+  // layout: [stages][q slots 2][conv][merge][unit info 2][barriers]
+  static constexpr int kOffQ = kStages * kStageBytes;
+  static constexpr int kOffConv = kOffQ + 2 * kQBytes;
+  static constexpr int kOffMerge = kOffConv + kConvBytes;
+  static constexpr int kOffInfo = kOffMerge + kMergeBytes;
+  static constexpr int kOffBar = kOffInfo + 2 * (int)sizeof(DecodeUnit);
+  static constexpr int kBytes = kOffBar + (2 * kStages + 4) * 8 + 1024;  // + base alignment
 };
 
-// Issue the loads of one stage: keys [kb, kb + kBN) clipped to [k_begin, k_end).
-// Cached keys (j < ctx) come from pages; the new key (j >= ctx) from the inputs.
-template <int D, bool FP8>
-__device__ __forceinline__ void load_stage(const AttnArgs& a, uint8_t* stage, int seq, int h,
-                                           int kb, int k_begin, int k_end, int ctx, int q0,
-                                           int tid) {
-  using S = Smem<D, FP8>;
-  constexpr int kChunks = S::kRowBytes / 16;  // per key row
-  const int Hkv = a.kv.p.num_kv_heads;
-  for (int idx = tid; idx < kBN * 2 * kChunks; idx += kThreads) {
-    const int key = idx / (2 * kChunks);
-    const int rem = idx % (2 * kChunks);
-    const int kv = rem / kChunks, c = rem % kChunks;
-    const int j = kb + key;
-    uint8_t* tile = stage + kv * kBN * S::kRowBytes;
-    const uint32_t dst_off = FP8 ? (uint32_t)(key * S::kRowBytes + c * 16) : swz(key, c, S::kRowBytes);
-    if (j < k_begin || j >= k_end) {
-      *reinterpret_cast<uint4*>(tile + dst_off) = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    if (j < ctx) {
-      const int32_t page = lookup_page(a.kv, seq, j);
-      if (page < 0) {
-        *reinterpret_cast<uint4*>(tile + dst_off) = make_uint4(0, 0, 0, 0);
-        continue;
-      }
-      const uint8_t* src =
-          a.kv.cache + pool_offset(a.kv.p, page, j % a.kv.p.page_size, 2 * h + kv, S::kElem) + c * 16;
-      cp_async_16(smem_u32(tile + dst_off), src);
-    } else {
-      const __nv_bfloat16* in = (kv ? a.kv.values : a.kv.keys) +
-                                ((int64_t)(q0 + (j - ctx)) * Hkv + h) * D;
-      if (FP8) {
-        // 16 codes = two 8-value bf16 chunks, quantised exactly as the page write does
-        const float scale = kv ? a.kv.p.v_scale : a.kv.p.k_scale;
-        const uint2 lo = quantize8(__ldg(reinterpret_cast<const uint4*>(in + c * 16)), scale);
-        const uint2 hi = quantize8(__ldg(reinterpret_cast<const uint4*>(in + c * 16 + 8)), scale);
-        *reinterpret_cast<uint4*>(tile + dst_off) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-      } else {
-        cp_async_16(smem_u32(tile + dst_off), in + c * 8);
-      }
-    }
-  }
+struct DecodeMaps {
+  CUtensorMap cache;  // pool [num_pages*P][2*Hkv][D]
+};
+
+// Address of 16-byte chunk `c` (of D/8) of key row `r` in a bf16 stage tile
+// written by 128-byte swizzled boxes (one box per 64-wide half).
+template <int D>
+__device__ __forceinline__ uint32_t stage_addr(uint32_t tile, int r, int c) {
+  return tile + (uint32_t)((c >> 3) * kBN * 128) + sw128(r, c & 7);
 }
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
-  using S = Smem<D, FP8>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sQ = smem;
-  uint8_t* sStages = smem + S::kQBytes;
-  uint8_t* sConv = sStages + S::kStagesBytes;
-  float* sMerge = reinterpret_cast<float*>(smem + S::kQBytes);  // reused after the loop
-  __shared__ int s_unit, s_last;
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ DecodeMaps maps, AttnArgs a) {
+  using C = Cfg<D, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t s_base = smem_u32(smem);
+  DecodeUnit* info = reinterpret_cast<DecodeUnit*>(smem + C::kOffInfo);
+  float* sMerge = reinterpret_cast<float*>(smem + C::kOffMerge);
+  const uint32_t bar_full = s_base + C::kOffBar;                 // [kStages]
+  const uint32_t bar_empty = bar_full + 8 * C::kStages;          // [kStages]
+  const uint32_t bar_qfull = bar_empty + 8 * C::kStages;         // [2]
+  const uint32_t bar_qempty = bar_qfull + 16;                    // [2]
+  __shared__ int s_abort, s_last;
 
   const rpa_params_t& p = a.kv.p;
   int32_t* hdr = a.kv.ws;
@@ -105,89 +94,172 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
   float2* part_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(hdr) + L.partial_ml_off);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gq = lane >> 2, tq = lane & 3;
   const int G = p.num_q_heads / p.num_kv_heads;
-  const int n_units = hdr[kHdrNumDecode];
+  const int P = p.page_size;
+
+  // zero both query slots (rows >= G stay zero), init barriers
+  for (int i = tid; i < 2 * C::kQBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + C::kOffQ)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    s_abort = 0;
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kConsumerWarps);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_qfull + 8 * s, 1);
+      mbar_init(bar_qempty + 8 * s, kConsumerWarps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    prefetch_tensormap(&maps.cache);
+    const int n_units = hdr[kHdrNumDecode];
+    uint32_t g = 0;  // stages issued so far
+    bool ok = true;
+    for (uint32_t uq = 0; ok; ++uq) {
+      const int slot = uq & 1;
+      const int u = atomicAdd(hdr + kHdrDecodeNext, 1);
+      if (!mbar_wait(bar_qempty + 8 * slot, ((uq >> 1) & 1) ^ 1, &s_abort)) {
+        ok = false;
+        break;
+      }
+      if (u >= n_units) {
+        info[slot].seq = -1;
+        mbar_arrive(bar_qfull + 8 * slot);
+        break;
+      }
+      DecodeUnit du = units[u];
+      du.pad = u;  // consumers need the unit's index for its partial results
+      info[slot] = du;
+      const int q0 = a.qsl[du.seq];
+      const uint32_t qbytes = (uint32_t)(G * D * 2);
+      mbar_arrive_expect_tx(bar_qfull + 8 * slot, qbytes);
+      bulk_load(s_base + C::kOffQ + slot * C::kQBytes,
+                a.queries + ((int64_t)q0 * p.num_q_heads + du.head * G) * D, qbytes,
+                bar_qfull + 8 * slot);
+      const int kb0 = du.k_begin & ~(kBN - 1);
+      const int n_st = (du.k_end - kb0 + kBN - 1) / kBN;
+      for (int st = 0; st < n_st; ++st, ++g) {
+        const int s = g % C::kStages;
+        if (!mbar_wait(bar_empty + 8 * s, ((g / C::kStages) & 1) ^ 1, &s_abort)) {
+          ok = false;
+          break;
+        }
+        const int kb = kb0 + st * kBN;
+        const int lo = max(kb, du.k_begin), hi = min(kb + kBN, du.k_end);
+        const int rows = P < kBN ? P : kBN;
+        const int pg0 = lo / P, pg1 = (hi - 1) / P;
+        const uint32_t bytes = (uint32_t)((pg1 - pg0 + 1) * rows * C::kRowBytes * C::kHalves * 2);
+        mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
+        const uint32_t stage = s_base + s * C::kStageBytes;
+        for (int pg = pg0; pg <= pg1; ++pg) {
+          int page = __ldg(a.kv.block_tables + (int64_t)du.seq * p.pages_per_seq + pg);
+          if (page < 0 || page >= p.num_pages) {
+            set_status(hdr, RPA_STATUS_BAD_PAGE);
+            page = 0;  // keep the byte count; the data is never trusted
+          }
+          const int row_in_stage = P < kBN ? pg * P - kb : 0;
+          const int z = page * P + (P < kBN ? 0 : kb % P);
+          for (int kv = 0; kv < 2; ++kv)
+            for (int hf = 0; hf < C::kHalves; ++hf)
+              tma_load_3d(stage + kv * C::kKVBytes + hf * C::kHalfBytes + row_in_stage * C::kRowBytes,
+                          &maps.cache, bar_full + 8 * s, FP8 ? 0 : hf * 64, 2 * du.head + kv, z);
+        }
+      }
+    }
+    if (!ok) {
+      set_status(hdr, RPA_STATUS_TIMEOUT);
+      s_abort = 1;
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int gq = lane >> 2, tq = lane & 3;
   const LogitXform xf{p.softmax_scale * p.k_scale, p.logits_soft_cap,
                       p.logits_soft_cap > 0.f ? 1.f / p.logits_soft_cap : 0.f,
                       p.softmax_scale * p.k_scale * kLog2e};
-
-  if (tid == 0) s_unit = atomicAdd(hdr + kHdrDecodeNext, 1);
-  __syncthreads();
-  int u = s_unit;
-  while (u < n_units) {
-    int next = 0;
-    if (tid == 0) next = atomicAdd(hdr + kHdrDecodeNext, 1);  // prefetch the next unit
-    const DecodeUnit du = units[u];
+  uint32_t g = 0;
+  for (uint32_t uq = 0;; ++uq) {
+    const int slot = uq & 1;
+    if (!mbar_wait(bar_qfull + 8 * slot, (uq >> 1) & 1, &s_abort)) {
+      set_status(hdr, RPA_STATUS_TIMEOUT);
+      s_abort = 1;
+      break;
+    }
+    const DecodeUnit du = info[slot];
+    if (du.seq < 0) break;
     const int seq = du.seq, h = du.head;
     const int q0 = a.qsl[seq];
-    const int kv_len = a.kv_lens[seq];
-    const int ctx = kv_len - 1;
+    const int ctx = a.kv_lens[seq] - 1;
 
     // split 0 stores the new token's key/value into its page
     if (du.split == 0 && warp == 0) write_token_kv<FP8>(a.kv, seq, q0, ctx, h, lane);
 
-    // Q tile: rows = the G q-heads of kv head h (rows >= G are zero)
-    for (int idx = tid; idx < kDecodeRows * (D / 8); idx += kThreads) {
-      const int r = idx / (D / 8), c = idx % (D / 8);
-      uint8_t* dst = sQ + swz(r, c, D * 2);
-      if (r < G) {
-        cp_async_16(smem_u32(dst), a.queries + ((int64_t)q0 * p.num_q_heads + h * G + r) * D + c * 8);
-      } else {
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    const int kb0 = du.k_begin;
-    const int n_stages = (du.k_end - du.k_begin + kBN - 1) / kBN;
+    uint32_t qa[D / 16][4];
+    {
+      const uint32_t sq = s_base + C::kOffQ + slot * C::kQBytes;
 #pragma unroll
-    for (int st = 0; st < kStages - 1; ++st) {
-      if (st < n_stages)
-        load_stage<D, FP8>(a, sStages + st * S::kStageBytes, seq, h, kb0 + st * kBN, du.k_begin,
-                           du.k_end, ctx, q0, tid);
-      cp_async_commit();
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int mi = lane >> 3;
+        const int row = (lane & 7) + ((mi & 1) << 3);
+        const int col = (2 * ks + (mi >> 1)) * 16;
+        ldmatrix_x4(sq + row * (D * 2) + col, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_qempty + 8 * slot);
     }
 
     float o[D / 8][4];
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    uint32_t qa[D / 16][4];
 
-    for (int st = 0; st < n_stages; ++st) {
-      cp_async_wait<kStages - 2>();
-      __syncthreads();
-      if (st == 0) {
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int mi = lane >> 3;
-          const int row = (lane & 7) + ((mi & 1) << 3);
-          const int chunk = 2 * ks + (mi >> 1);
-          ldmatrix_x4(smem_u32(sQ + swz(row, chunk, D * 2)), qa[ks][0], qa[ks][1], qa[ks][2],
-                      qa[ks][3]);
-        }
+    const int kb0 = du.k_begin & ~(kBN - 1);
+    const int n_st = (du.k_end - kb0 + kBN - 1) / kBN;
+    bool ok = true;
+    for (int st = 0; st < n_st; ++st, ++g) {
+      const int s = g % C::kStages;
+      if (!mbar_wait(bar_full + 8 * s, (g / C::kStages) & 1, &s_abort)) {
+        ok = false;
+        break;
       }
-      {
-        const int nst = st + kStages - 1;
-        if (nst < n_stages)
-          load_stage<D, FP8>(a, sStages + (nst % kStages) * S::kStageBytes, seq, h,
-                             kb0 + nst * kBN, du.k_begin, du.k_end, ctx, q0, tid);
-        cp_async_commit();
-      }
-      const uint8_t* stage = sStages + (st % kStages) * S::kStageBytes;
-      const uint8_t* tK;
-      const uint8_t* tV;
-      int krow0;  // first row of this warp's keys in tK/tV
+      const uint32_t stage = s_base + s * C::kStageBytes;
+      const int kw = kb0 + st * kBN + warp * kKeysPerWarp;  // this warp's first key
+      uint32_t tK, tV;
+      int krow0;
+      bool wrote = false;
       if (FP8) {
-        // convert this warp's 16 keys and values to bf16 (exact) in its own buffer
-        uint8_t* cK = sConv + warp * 2 * kKeysPerWarp * D * 2;
-        uint8_t* cV = cK + kKeysPerWarp * D * 2;
+        // convert this warp's 16 keys/values to bf16 in its own buffer; keys
+        // outside the unit become zero, the new token comes from the inputs
+        const uint32_t cK = s_base + C::kOffConv + warp * 2 * kKeysPerWarp * D * 2;
+        const uint32_t cV = cK + kKeysPerWarp * D * 2;
+        uint8_t* gK = smem + (cK - s_base);
+        uint8_t* gV = smem + (cV - s_base);
         for (int idx = lane; idx < 2 * kKeysPerWarp * (D / 8); idx += 32) {
           const int kv = idx / (kKeysPerWarp * (D / 8));
           const int rem = idx % (kKeysPerWarp * (D / 8));
           const int r = rem / (D / 8), c = rem % (D / 8);
-          const uint2 codes = *reinterpret_cast<const uint2*>(
-              stage + kv * kBN * S::kRowBytes + (warp * kKeysPerWarp + r) * S::kRowBytes + c * 8);
-          *reinterpret_cast<uint4*>((kv ? cV : cK) + swz(r, c, D * 2)) = dequant8(codes);
+          const int j = kw + r;
+          uint4 val;
+          if (j < du.k_begin || j >= du.k_end) {
+            val = make_uint4(0, 0, 0, 0);
+          } else if (j == ctx) {
+            const __nv_bfloat16* in = (kv ? a.kv.values : a.kv.keys) +
+                                      ((int64_t)q0 * p.num_kv_heads + h) * D + c * 8;
+            val = dequant8(quantize8(__ldg(reinterpret_cast<const uint4*>(in)),
+                                     kv ? p.v_scale : p.k_scale));
+          } else {
+            const uint2 codes = *reinterpret_cast<const uint2*>(
+                smem + (stage - s_base) + kv * C::kKVBytes + (warp * kKeysPerWarp + r) * C::kRowBytes + c * 8);
+            val = dequant8(codes);
+          }
+          *reinterpret_cast<uint4*>((kv ? gV : gK) + swz(r, c, D * 2)) = val;
         }
         __syncwarp();
         tK = cK;
@@ -195,83 +267,119 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
         krow0 = 0;
       } else {
         tK = stage;
-        tV = stage + kBN * S::kRowBytes;
+        tV = stage + C::kKVBytes;
         krow0 = warp * kKeysPerWarp;
+        // rows outside [k_begin, k_end): zero the values (masked keys may hold
+        // anything, and 0 * NaN would poison P V); the new token's row: inputs
+        const bool edge = kw < du.k_begin || kw + kKeysPerWarp > du.k_end ||
+                          (ctx >= kw && ctx < kw + kKeysPerWarp);
+        if (edge) {
+          for (int idx = lane; idx < kKeysPerWarp * (D / 8); idx += 32) {
+            const int r = idx / (D / 8), c = idx % (D / 8);
+            const int j = kw + r;
+            if (j < du.k_begin || j >= du.k_end) {
+              *reinterpret_cast<uint4*>(smem + (stage_addr<D>(tV, krow0 + r, c) - s_base)) =
+                  make_uint4(0, 0, 0, 0);
+            } else if (j == ctx) {
+              const int64_t off = ((int64_t)q0 * p.num_kv_heads + h) * D + c * 8;
+              *reinterpret_cast<uint4*>(smem + (stage_addr<D>(tK, krow0 + r, c) - s_base)) =
+                  __ldg(reinterpret_cast<const uint4*>(a.kv.keys + off));
+              *reinterpret_cast<uint4*>(smem + (stage_addr<D>(tV, krow0 + r, c) - s_base)) =
+                  __ldg(reinterpret_cast<const uint4*>(a.kv.values + off));
+            }
+          }
+          wrote = true;
+          __syncwarp();
+        }
       }
 
       // S = Q K^T for this warp's 16 keys (two n8 tiles)
-      float s[2][4];
+      float sc[2][4];
 #pragma unroll
-      for (int n = 0; n < 2; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+      for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const int mi = lane >> 3;
         const int key = krow0 + (lane & 7) + ((mi >> 1) << 3);
         const int chunk = 2 * ks + (mi & 1);
+        const uint32_t addr = FP8 ? tK + swz(key, chunk, D * 2) : stage_addr<D>(tK, key, chunk);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(smem_u32(tK + swz(key, chunk, D * 2)), b0, b1, b2, b3);
-        mma_bf16_16816(s[0], qa[ks], b0, b1);
-        mma_bf16_16816(s[1], qa[ks], b2, b3);
+        ldmatrix_x4(addr, b0, b1, b2, b3);
+        mma_bf16_16816(sc[0], qa[ks], b0, b1);
+        mma_bf16_16816(sc[1], qa[ks], b2, b3);
       }
       // logits, mask, online softmax (rows gq and gq + 8)
-      const int kw = kb0 + st * kBN + warp * kKeysPerWarp;
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = kw + n * 8 + 2 * tq + (e & 1);
-          const float x = (j >= du.k_begin && j < du.k_end) ? xf(s[n][e]) : -INFINITY;
-          s[n][e] = x;
+          const float x = (j >= du.k_begin && j < du.k_end) ? xf(sc[n][e]) : -INFINITY;
+          sc[n][e] = x;
           mx[e >> 1] = fmaxf(mx[e >> 1], x);
         }
-      float alpha[2], msafe[2];
+      float alpha[2];
+      bool rescale = false;
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const float mnew = fmaxf(m_run[r], quad_max(mx[r]));
-        msafe[r] = mnew == -INFINITY ? 0.f : mnew;
-        alpha[r] = exp2f(m_run[r] - msafe[r]);
-        m_run[r] = mnew;
+        const float mt = quad_max(mx[r]);
+        alpha[r] = 1.f;
+        if (mt > m_run[r] + (float)kRescaleLog2) {  // also true on the first finite tile
+          alpha[r] = m_run[r] == -INFINITY ? 0.f : exp2f(m_run[r] - mt);
+          m_run[r] = mt;
+          rescale = true;
+        }
       }
       float rs[2] = {0.f, 0.f};
+      const float ms0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+      const float ms1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float pe = exp2f(s[n][e] - msafe[e >> 1]);
-          s[n][e] = pe;
+          const float pe = exp2f(sc[n][e] - ((e >> 1) ? ms1 : ms0));
+          sc[n][e] = pe;
           rs[e >> 1] += pe;
         }
+      if (rescale) {
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+          o[n][0] *= alpha[0];
+          o[n][1] *= alpha[0];
+          o[n][2] *= alpha[1];
+          o[n][3] *= alpha[1];
+        }
+      }
 #pragma unroll
       for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + rs[r];
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= alpha[0];
-        o[n][1] *= alpha[0];
-        o[n][2] *= alpha[1];
-        o[n][3] *= alpha[1];
-      }
-      // O += P V (P as the A operand straight from the score registers)
       uint32_t pa[4];
-      pa[0] = pack_bf16(s[0][0], s[0][1]);
-      pa[1] = pack_bf16(s[0][2], s[0][3]);
-      pa[2] = pack_bf16(s[1][0], s[1][1]);
-      pa[3] = pack_bf16(s[1][2], s[1][3]);
+      pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+      pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+      pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+      pa[3] = pack_bf16(sc[1][2], sc[1][3]);
 #pragma unroll
       for (int cp = 0; cp < D / 16; ++cp) {
         const int mi = lane >> 3;
         const int key = krow0 + (lane & 7) + ((mi & 1) << 3);
         const int chunk = 2 * cp + (mi >> 1);
+        const uint32_t addr = FP8 ? tV + swz(key, chunk, D * 2) : stage_addr<D>(tV, key, chunk);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(smem_u32(tV + swz(key, chunk, D * 2)), b0, b1, b2, b3);
+        ldmatrix_x4_trans(addr, b0, b1, b2, b3);
         mma_bf16_16816(o[2 * cp], pa, b0, b1);
         mma_bf16_16816(o[2 * cp + 1], pa, b2, b3);
       }
+      if (wrote) fence_proxy_async();  // our stores precede the next TMA into this stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
-    cp_async_wait<0>();
-    __syncthreads();  // stage memory becomes the merge area
+    if (!ok) {
+      set_status(hdr, RPA_STATUS_TIMEOUT);
+      s_abort = 1;
+      break;
+    }
 
-    // per-warp state -> shared memory: rows [warp][16] of (m, l, O[D])
+    // per-warp state -> shared memory rows [warp][16] of (m, l, O[D])
     {
       float* mw = sMerge + warp * kDecodeRows * (D + 2);
       const float l0 = quad_sum(l_run[0]), l1 = quad_sum(l_run[1]);
@@ -290,33 +398,33 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
         mw[(gq + 8) * (D + 2) + 2 + d + 1] = o[n][3];
       }
     }
-    __syncthreads();
+    named_bar(1, kConsumerWarps * 32);
 
-    // merge the four warps; one (row, 4 dims) per thread-iteration
     const bool single = du.nsplit == 1;
-    for (int idx = tid; idx < G * (D / 4); idx += kThreads) {
+    const int ctid = tid;  // consumers are threads 0..127
+    for (int idx = ctid; idx < G * (D / 4); idx += kConsumerWarps * 32) {
       const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sMerge[(w * kDecodeRows + r) * (D + 2)]);
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sMerge[(w * kDecodeRows + r) * (D + 2)]);
       float Lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < kConsumerWarps; ++w) {
         const float* row = sMerge + (w * kDecodeRows + r) * (D + 2);
-        const float sc = row[0] == -INFINITY ? 0.f : exp2f(row[0] - M);
-        Lsum += sc * row[1];
+        const float scw = row[0] == -INFINITY ? 0.f : exp2f(row[0] - M);
+        Lsum += scw * row[1];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += sc * row[2 + d + e];
+        for (int e = 0; e < 4; ++e) acc[e] += scw * row[2 + d + e];
       }
       const int hq = h * G + r;
       if (single) {
         if (a.sink) {
           const float sk = a.sink[hq] * kLog2e;
           const float M2 = fmaxf(M, sk);
-          const float sc = exp2f(M - M2);
-          Lsum = Lsum * sc + exp2f(sk - M2);
+          const float scs = exp2f(M - M2);
+          Lsum = Lsum * scs + exp2f(sk - M2);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[e] *= sc;
+          for (int e = 0; e < 4; ++e) acc[e] *= scs;
         }
         const float inv = p.v_scale / Lsum;
         __nv_bfloat16* dst = a.out + ((int64_t)q0 * p.num_q_heads + hq) * D + d;
@@ -325,6 +433,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
         pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
         *reinterpret_cast<uint2*>(dst) = pk;
       } else {
+        const int u = du.pad;  // this unit's index (set by the producer)
         float* po = part_o + ((int64_t)u * G + r) * D + d;
         *reinterpret_cast<float4*>(po) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         if (d == 0) part_ml[(int64_t)u * G + r] = make_float2(M, Lsum);
@@ -334,15 +443,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
     if (!single) {
       // the last split of (seq, head) to finish combines all of them
       __threadfence();
-      __syncthreads();
-      if (tid == 0) {
+      named_bar(1, kConsumerWarps * 32);
+      if (ctid == 0) {
         const int prev = atomicAdd(counters + (int64_t)seq * p.num_kv_heads + h, 1);
         s_last = prev == du.nsplit - 1;
       }
-      __syncthreads();
+      named_bar(1, kConsumerWarps * 32);
       if (s_last) {
         __threadfence();
-        for (int idx = tid; idx < G * (D / 4); idx += kThreads) {
+        for (int idx = ctid; idx < G * (D / 4); idx += kConsumerWarps * 32) {
           const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
           const int hq = h * G + r;
           float M = a.sink ? a.sink[hq] * kLog2e : -INFINITY;
@@ -353,13 +462,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
           for (int k = 0; k < du.nsplit; ++k) {
             const int64_t pu = (int64_t)(du.first_unit + k) * G + r;
             const float2 ml = __ldcg(&part_ml[pu]);
-            const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-            Lsum += sc * ml.y;
+            const float scs = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+            Lsum += scs * ml.y;
             const float4 po = __ldcg(reinterpret_cast<const float4*>(part_o + pu * D + d));
-            acc[0] += sc * po.x;
-            acc[1] += sc * po.y;
-            acc[2] += sc * po.z;
-            acc[3] += sc * po.w;
+            acc[0] += scs * po.x;
+            acc[1] += scs * po.y;
+            acc[2] += scs * po.z;
+            acc[3] += scs * po.w;
           }
           const float inv = p.v_scale / Lsum;
           __nv_bfloat16* dst = a.out + ((int64_t)q0 * p.num_q_heads + hq) * D + d;
@@ -370,10 +479,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
         }
       }
     }
-    __syncthreads();
-    if (tid == 0) s_unit = next;
-    __syncthreads();
-    u = s_unit;
+    named_bar(1, kConsumerWarps * 32);  // the merge area is rewritten by the next unit
   }
 }
 
@@ -382,18 +488,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
 template <int D, bool FP8>
 static cudaError_t launch_decode_t(const AttnArgs& a, int max_units, int num_sms,
                                    cudaStream_t stream) {
-  using S = dec::Smem<D, FP8>;
+  using C = dec::Cfg<D, FP8>;
+  static std::atomic<unsigned long long> attr_done{0};
   auto kern = dec::decode_kernel<D, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kBytes, &attr_done);
   if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, dec::kThreads, S::kBytes);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  int grid = num_sms * per_sm;
+  const rpa_params_t& p = a.kv.p;
+  dec::DecodeMaps maps;
+  const uint32_t rows = p.page_size < dec::kBN ? (uint32_t)p.page_size : (uint32_t)dec::kBN;
+  if (!encode_map_3d(&maps.cache, a.kv.cache, FP8 ? 1 : 2, (uint64_t)D,
+                     2 * (uint64_t)p.num_kv_heads, (uint64_t)p.num_pages * p.page_size,
+                     FP8 ? (uint32_t)D : 64u, 1u, rows, !FP8))
+    return cudaErrorInvalidValue;
+  int grid = num_sms;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
-  kern<<<grid, dec::kThreads, S::kBytes, stream>>>(a);
+  kern<<<grid, dec::kThreads, C::kBytes, stream>>>(maps, a);
   return cudaGetLastError();
 }
 

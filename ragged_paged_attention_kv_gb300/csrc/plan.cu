@@ -113,11 +113,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
     if (sp.flags) atomicOr(&s_flags, sp.flags);
     if (sp.cls == 1) my_keys += (unsigned long long)(sp.kv_len - sp.lo);
   }
-  atomicAdd(&s_keys, my_keys);
+  // warp sums first: one shared atomic per warp, not per thread
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) my_keys += __shfl_xor_sync(0xffffffffu, my_keys, o);
+  if ((tid & 31) == 0 && my_keys) atomicAdd(&s_keys, my_keys);
   __syncthreads();
   const unsigned long long want =
       (s_keys * (unsigned long long)Hkv + kDecodeUnitsTarget - 1) / kDecodeUnitsTarget;
-  int chunk = (int)((want + 15) / 16 * 16);
+  // splits are whole 64-key stages of the decode kernel
+  int chunk = (int)((want + 63) / 64 * 64);
   if (chunk < kDecodeChunkMin) chunk = kDecodeChunkMin;
 
   // Pass 2: emit units in sequence order (prefill tiles last-first, so the
@@ -129,7 +133,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
     int nsplit = 0, ntiles = 0;
     if (s < S) {
       sp = classify(p, s, d0, kv_lens, qsl);  // flags were taken in pass 1
-      if (sp.cls == 1) nsplit = (sp.kv_len - sp.lo + chunk - 1) / chunk;
+      if (sp.cls == 1) nsplit = (sp.kv_len - (sp.lo & ~63) + chunk - 1) / chunk;
       if (sp.cls == 2) ntiles = (sp.q_len + tile_tokens - 1) / tile_tokens;
     }
     int dec_total, pf_total;
@@ -143,8 +147,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
           DecodeUnit u;
           u.seq = s;
           u.head = h;
-          u.k_begin = sp.lo + k * chunk;
-          u.k_end = min(sp.kv_len, sp.lo + (k + 1) * chunk);
+          const int base = sp.lo & ~63;  // split boundaries on 64-key stages
+          u.k_begin = max(sp.lo, base + k * chunk);
+          u.k_end = min(sp.kv_len, base + (k + 1) * chunk);
           u.split = k;
           u.nsplit = nsplit;
           u.first_unit = first;

@@ -12,6 +12,7 @@
 // window masks applied only on tiles that cross a mask edge.
 #include "common.cuh"
 #include "kv_write.cuh"
+#include "tma_host.h"
 
 namespace rpa {
 
@@ -291,12 +292,17 @@ static cudaError_t launch_prefill_t(const AttnArgs& a, int max_units, int num_sm
                                     cudaStream_t stream) {
   using S = pf::Smem<D>;
   auto kern = pf::prefill_kernel<D, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+  static std::atomic<unsigned long long> attr_done{0};
+  static std::atomic<int> per_sm_cached{0};
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), S::kBytes, &attr_done);
   if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, pf::kThreads, S::kBytes);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
+  int per_sm = per_sm_cached.load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, pf::kThreads, S::kBytes);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    per_sm_cached.store(per_sm, std::memory_order_relaxed);
+  }
   int grid = num_sms * per_sm;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
