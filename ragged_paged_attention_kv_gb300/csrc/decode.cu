@@ -53,9 +53,17 @@ struct Cfg {
   static constexpr int kOffConv = kOffQ + 2 * kQBytes;
   static constexpr int kOffMerge = kOffConv + kConvBytes;
   static constexpr int kOffInfo = kOffMerge + kMergeBytes;
-  static constexpr int kOffBar = kOffInfo + 2 * (int)sizeof(DecodeUnit);
+  static constexpr int kOffBar = kOffInfo + 2 * 64;  // two UnitInfo slots
   static constexpr int kBytes = kOffBar + (2 * kStages + 4) * 8 + 1024;  // + base alignment
 };
+
+// What the producer tells the consumers about the unit in a query slot.
+struct UnitInfo {
+  DecodeUnit du;  // du.pad holds the unit's index; du.seq < 0 means "no more units"
+  int q0, ctx;    // the sequence's token row and the new token's position
+  int pad[6];
+};
+static_assert(sizeof(UnitInfo) == 64, "two UnitInfo slots take 128 bytes");
 
 struct DecodeMaps {
   CUtensorMap cache;  // pool [num_pages*P][2*Hkv][D]
@@ -76,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t s_base = smem_u32(smem);
-  DecodeUnit* info = reinterpret_cast<DecodeUnit*>(smem + C::kOffInfo);
+  UnitInfo* info = reinterpret_cast<UnitInfo*>(smem + C::kOffInfo);
   float* sMerge = reinterpret_cast<float*>(smem + C::kOffMerge);
   const uint32_t bar_full = s_base + C::kOffBar;                 // [kStages]
   const uint32_t bar_empty = bar_full + 8 * C::kStages;          // [kStages]
@@ -116,54 +124,96 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane != 0) return;
-    prefetch_tensormap(&maps.cache);
+    // The whole warp runs the loop; lane l looks up and copies pages l and
+    // l + 32 of each stage, with the page ids of the next stage loaded while
+    // the current one waits for a free slot.
+    if (lane == 0) prefetch_tensormap(&maps.cache);
     const int n_units = hdr[kHdrNumDecode];
-    uint32_t g = 0;  // stages issued so far
+    const int rows = P < kBN ? P : kBN;  // rows of one box
+    uint32_t g = 0;                      // stages issued so far
     bool ok = true;
     for (uint32_t uq = 0; ok; ++uq) {
       const int slot = uq & 1;
-      const int u = atomicAdd(hdr + kHdrDecodeNext, 1);
+      int u = 0;
+      if (lane == 0) u = atomicAdd(hdr + kHdrDecodeNext, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      DecodeUnit du{};
+      int q0 = 0, kv_len = 0;
+      if (u < n_units) {
+        du = units[u];
+        q0 = a.qsl[du.seq];
+        kv_len = a.kv_lens[du.seq];
+      }
+      const int kb0 = du.k_begin & ~(kBN - 1);
+      const int n_st = u < n_units ? (du.k_end - kb0 + kBN - 1) / kBN : 0;
+      const int64_t bt_row = (int64_t)du.seq * p.pages_per_seq;
+      auto stage_pages = [&](int st, int& pg0, int& npg) {
+        const int kb = kb0 + st * kBN;
+        const int lo = max(kb, du.k_begin), hi = min(kb + kBN, du.k_end);
+        pg0 = lo / P;
+        npg = (hi - 1) / P - pg0 + 1;
+      };
+      auto load_ids = [&](int st, int* ids) {
+        int pg0, npg;
+        stage_pages(st, pg0, npg);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int k = lane + 32 * i;
+          ids[i] = k < npg ? __ldg(a.kv.block_tables + bt_row + pg0 + k) : 0;
+        }
+      };
+      int ids_next[2] = {0, 0};
+      if (n_st > 0) load_ids(0, ids_next);
       if (!mbar_wait(bar_qempty + 8 * slot, ((uq >> 1) & 1) ^ 1, &s_abort)) {
         ok = false;
         break;
       }
       if (u >= n_units) {
-        info[slot].seq = -1;
-        mbar_arrive(bar_qfull + 8 * slot);
+        if (lane == 0) {
+          info[slot].du.seq = -1;
+          mbar_arrive(bar_qfull + 8 * slot);
+        }
         break;
       }
-      DecodeUnit du = units[u];
-      du.pad = u;  // consumers need the unit's index for its partial results
-      info[slot] = du;
-      const int q0 = a.qsl[du.seq];
-      const uint32_t qbytes = (uint32_t)(G * D * 2);
-      mbar_arrive_expect_tx(bar_qfull + 8 * slot, qbytes);
-      bulk_load(s_base + C::kOffQ + slot * C::kQBytes,
-                a.queries + ((int64_t)q0 * p.num_q_heads + du.head * G) * D, qbytes,
-                bar_qfull + 8 * slot);
-      const int kb0 = du.k_begin & ~(kBN - 1);
-      const int n_st = (du.k_end - kb0 + kBN - 1) / kBN;
+      if (lane == 0) {
+        UnitInfo ui;
+        ui.du = du;
+        ui.du.pad = u;  // consumers need the unit's index for its partial results
+        ui.q0 = q0;
+        ui.ctx = kv_len - 1;
+        info[slot] = ui;
+        const uint32_t qbytes = (uint32_t)(G * D * 2);
+        mbar_arrive_expect_tx(bar_qfull + 8 * slot, qbytes);
+        bulk_load(s_base + C::kOffQ + slot * C::kQBytes,
+                  a.queries + ((int64_t)q0 * p.num_q_heads + du.head * G) * D, qbytes,
+                  bar_qfull + 8 * slot);
+      }
       for (int st = 0; st < n_st; ++st, ++g) {
+        int ids[2] = {ids_next[0], ids_next[1]};
+        if (st + 1 < n_st) load_ids(st + 1, ids_next);
         const int s = g % C::kStages;
         if (!mbar_wait(bar_empty + 8 * s, ((g / C::kStages) & 1) ^ 1, &s_abort)) {
           ok = false;
           break;
         }
+        int pg0, npg;
+        stage_pages(st, pg0, npg);
         const int kb = kb0 + st * kBN;
-        const int lo = max(kb, du.k_begin), hi = min(kb + kBN, du.k_end);
-        const int rows = P < kBN ? P : kBN;
-        const int pg0 = lo / P, pg1 = (hi - 1) / P;
-        const uint32_t bytes = (uint32_t)((pg1 - pg0 + 1) * rows * C::kRowBytes * C::kHalves * 2);
-        mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
+        if (lane == 0)
+          mbar_arrive_expect_tx(bar_full + 8 * s,
+                                (uint32_t)(npg * rows * C::kRowBytes * C::kHalves * 2));
+        __syncwarp();
         const uint32_t stage = s_base + s * C::kStageBytes;
-        for (int pg = pg0; pg <= pg1; ++pg) {
-          int page = __ldg(a.kv.block_tables + (int64_t)du.seq * p.pages_per_seq + pg);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int k = lane + 32 * i;
+          if (k >= npg) continue;
+          int page = ids[i];
           if (page < 0 || page >= p.num_pages) {
             set_status(hdr, RPA_STATUS_BAD_PAGE);
             page = 0;  // keep the byte count; the data is never trusted
           }
-          const int row_in_stage = P < kBN ? pg * P - kb : 0;
+          const int row_in_stage = P < kBN ? (pg0 + k) * P - kb : 0;
           const int z = page * P + (P < kBN ? 0 : kb % P);
           for (int kv = 0; kv < 2; ++kv)
             for (int hf = 0; hf < C::kHalves; ++hf)
@@ -172,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       set_status(hdr, RPA_STATUS_TIMEOUT);
       s_abort = 1;
     }
@@ -192,14 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_abort = 1;
       break;
     }
-    const DecodeUnit du = info[slot];
+    const DecodeUnit du = info[slot].du;
     if (du.seq < 0) break;
     const int seq = du.seq, h = du.head;
-    const int q0 = a.qsl[seq];
-    const int ctx = a.kv_lens[seq] - 1;
-
-    // split 0 stores the new token's key/value into its page
-    if (du.split == 0 && warp == 0) write_token_kv<FP8>(a.kv, seq, q0, ctx, h, lane);
+    const int q0 = info[slot].q0;
+    const int ctx = info[slot].ctx;
 
     uint32_t qa[D / 16][4];
     {
@@ -379,6 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       break;
     }
 
+    // split 0 stores the new token's key/value into its page
+    if (du.split == 0 && warp == 0) write_token_kv<FP8>(a.kv, seq, q0, ctx, h, lane);
+
     // per-warp state -> shared memory rows [warp][16] of (m, l, O[D])
     {
       float* mw = sMerge + warp * kDecodeRows * (D + 2);
@@ -442,15 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (!single) {
       // the last split of (seq, head) to finish combines all of them
-      __threadfence();
+      // publish: CTA barrier, then one thread fences and counts (the
+      // fence after the barrier covers every consumer's partial stores)
       named_bar(1, kConsumerWarps * 32);
       if (ctid == 0) {
+        __threadfence();
         const int prev = atomicAdd(counters + (int64_t)seq * p.num_kv_heads + h, 1);
         s_last = prev == du.nsplit - 1;
+        if (s_last) __threadfence();
       }
       named_bar(1, kConsumerWarps * 32);
       if (s_last) {
-        __threadfence();
         for (int idx = ctid; idx < G * (D / 4); idx += kConsumerWarps * 32) {
           const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
           const int hq = h * G + r;

@@ -44,6 +44,16 @@ __device__ int block_exclusive_scan(int v, int* total, int* smem /* 33 ints */) 
   return excl;
 }
 
+// Largest i < n with off[i] <= x (off is nondecreasing, off[0] == 0 <= x).
+__device__ __forceinline__ int last_at_or_below(const int* off, int n, int x) {
+  int lo = 0, hi = n;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
 struct SeqPlan {
   int cls;        // 0 none, 1 decode, 2 prefill
   int q0, q_len, kv_len, lo;
@@ -84,6 +94,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   __shared__ int s_flags;
   __shared__ int s_scan[33];
   __shared__ unsigned long long s_keys;
+  __shared__ int s_doff[kPlanThreads], s_poff[kPlanThreads], s_nsplit[kPlanThreads],
+      s_ntiles[kPlanThreads], s_lo[kPlanThreads], s_len[kPlanThreads];
   const WorkspaceLayout L(p);
   DecodeUnit* dunits = reinterpret_cast<DecodeUnit*>(reinterpret_cast<char*>(ws) + L.decode_units_off);
   PrefillUnit* punits =
@@ -124,8 +136,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   int chunk = (int)((want + 63) / 64 * 64);
   if (chunk < kDecodeChunkMin) chunk = kDecodeChunkMin;
 
-  // Pass 2: emit units in sequence order (prefill tiles last-first, so the
-  // longest causal tiles start first under the dynamic scheduler).
+  // Pass 2, per batch of kPlanThreads sequences: scan the unit counts, then
+  // emit the units cooperatively (one thread per unit, coalesced stores).
+  // Prefill units are ordered head-major, each head's tiles last-first, so the
+  // CTAs running at the same time share one head's keys in L2 and the longest
+  // causal tiles start first under the dynamic scheduler.
   int dec_base = 0, pf_base = 0;
   for (int base = 0; base < S; base += kPlanThreads) {
     const int s = base + tid;
@@ -137,41 +152,47 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
       if (sp.cls == 2) ntiles = (sp.q_len + tile_tokens - 1) / tile_tokens;
     }
     int dec_total, pf_total;
-    const int dec_off = dec_base + block_exclusive_scan(nsplit * Hkv, &dec_total, s_scan);
-    const int pf_off = pf_base + block_exclusive_scan(ntiles * Hkv, &pf_total, s_scan);
-    if (sp.cls == 1) {
-      for (int h = 0; h < Hkv; ++h) {
-        counters[(int64_t)s * Hkv + h] = 0;
-        const int first = dec_off + h * nsplit;
-        for (int k = 0; k < nsplit; ++k) {
-          DecodeUnit u;
-          u.seq = s;
-          u.head = h;
-          const int base = sp.lo & ~63;  // split boundaries on 64-key stages
-          u.k_begin = max(sp.lo, base + k * chunk);
-          u.k_end = min(sp.kv_len, base + (k + 1) * chunk);
-          u.split = k;
-          u.nsplit = nsplit;
-          u.first_unit = first;
-          u.pad = 0;
-          dunits[first + k] = u;
-        }
-      }
-    } else if (sp.cls == 2) {
-      for (int r = 0; r < ntiles; ++r) {
-        const int t = ntiles - 1 - r;
-        for (int h = 0; h < Hkv; ++h) {
-          PrefillUnit u;
-          u.seq = s;
-          u.t_begin = t * tile_tokens;
-          u.t_end = min(sp.q_len, (t + 1) * tile_tokens);
-          u.head = h;
-          punits[pf_off + r * Hkv + h] = u;
-        }
-      }
+    const int dec_off = block_exclusive_scan(nsplit * Hkv, &dec_total, s_scan);
+    const int pf_off = block_exclusive_scan(ntiles * Hkv, &pf_total, s_scan);
+    s_doff[tid] = dec_off;
+    s_poff[tid] = pf_off;
+    s_nsplit[tid] = nsplit;
+    s_ntiles[tid] = ntiles;
+    s_lo[tid] = sp.lo;
+    s_len[tid] = sp.cls == 1 ? sp.kv_len : sp.q_len;
+    __syncthreads();
+    for (int u = tid; u < dec_total; u += kPlanThreads) {
+      const int i = last_at_or_below(s_doff, kPlanThreads, u);
+      const int ns = s_nsplit[i], r = u - s_doff[i];
+      const int h = r / ns, k = r % ns;
+      const int lo = s_lo[i], kv = s_len[i];
+      const int stage0 = lo & ~63;  // split boundaries on 64-key stages
+      DecodeUnit du;
+      du.seq = base + i;
+      du.head = h;
+      du.k_begin = max(lo, stage0 + k * chunk);
+      du.k_end = min(kv, stage0 + (k + 1) * chunk);
+      du.split = k;
+      du.nsplit = ns;
+      du.first_unit = dec_base + s_doff[i] + h * ns;
+      du.pad = 0;
+      dunits[dec_base + u] = du;
+      if (k == 0) counters[(int64_t)(base + i) * Hkv + h] = 0;
+    }
+    for (int u = tid; u < pf_total; u += kPlanThreads) {
+      const int i = last_at_or_below(s_poff, kPlanThreads, u);
+      const int nt = s_ntiles[i], r = u - s_poff[i];
+      const int h = r / nt, t = nt - 1 - r % nt;
+      PrefillUnit pu;
+      pu.seq = base + i;
+      pu.t_begin = t * tile_tokens;
+      pu.t_end = min(s_len[i], (t + 1) * tile_tokens);
+      pu.head = h;
+      punits[pf_base + u] = pu;
     }
     dec_base += dec_total;
     pf_base += pf_total;
+    __syncthreads();  // the per-sequence arrays are rewritten by the next batch
   }
   __syncthreads();
   if (tid == 0) {
