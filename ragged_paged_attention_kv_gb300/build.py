@@ -33,8 +33,10 @@ def _nvcc() -> str:
 
 
 def _flags(extra=()):
+    # RPA_NVCC_DEFINES: extra -D options (e.g. "-DRPA_DECODE_UNITS_TARGET=2048") for tuning builds
+    defines = os.environ.get("RPA_NVCC_DEFINES", "").split()
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                   "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr", *extra]
+                   "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr", *defines, *extra]
 
 
 def _headers():

@@ -7,13 +7,9 @@
 #include "common.cuh"
 #include "kv_write.cuh"
 
+#include "launch.h"
+
 namespace rpa {
-cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int32_t* qsl,
-                        const int32_t* dist, int32_t* ws, cudaStream_t stream);
-cudaError_t launch_cache_write(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,
-                               int num_sms, cudaStream_t stream);
-cudaError_t launch_decode(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
-cudaError_t launch_prefill(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
 
 static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -65,6 +61,29 @@ static int num_sms_current() {
 
 using namespace rpa;
 
+namespace rpa {
+int enqueue_forward(const rpa_params_t& p, const AttnArgs& a, const int32_t* distribution,
+                    int num_sms, cudaStream_t s, void* const* events) {
+  const WorkspaceLayout L(p);
+  const bool tc = prefill_uses_tc(p);
+  auto mark = [&](int i) -> bool {
+    return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+  };
+  if (!mark(0)) return RPA_ERR_CUDA;
+  if (launch_plan(p, a.kv_lens, a.qsl, distribution, a.kv.ws, prefill_rows_for(p), s) !=
+      cudaSuccess)
+    return RPA_ERR_CUDA;
+  if (!mark(1)) return RPA_ERR_CUDA;
+  if (launch_decode(a, (int)L.max_decode_units, num_sms, s) != cudaSuccess) return RPA_ERR_CUDA;
+  if (!mark(2)) return RPA_ERR_CUDA;
+  const cudaError_t e = tc ? launch_prefill_tc(a, (int)L.max_prefill_units, num_sms, s)
+                           : launch_prefill(a, (int)L.max_prefill_units, num_sms, s);
+  if (e != cudaSuccess) return RPA_ERR_CUDA;
+  if (!mark(3)) return RPA_ERR_CUDA;
+  return RPA_OK;
+}
+}  // namespace rpa
+
 static int forward_impl(const rpa_params_t* params, const void* queries, const void* keys,
                         const void* values, void* kv_cache, const int32_t* kv_lens,
                         const int32_t* block_tables, const int32_t* query_start_loc,
@@ -80,29 +99,16 @@ static int forward_impl(const rpa_params_t* params, const void* queries, const v
   if (rc) return rc;
   const int sms = num_sms_current();
   if (sms <= 0) return RPA_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int32_t* ws = reinterpret_cast<int32_t*>(workspace);
-  const WorkspaceLayout L(*params);
-  auto mark = [&](int i) -> bool {
-    return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
-  };
-  if (!mark(0)) return RPA_ERR_CUDA;
-  if (launch_plan(*params, kv_lens, query_start_loc, distribution, ws, s) != cudaSuccess)
-    return RPA_ERR_CUDA;
-  if (!mark(1)) return RPA_ERR_CUDA;
   AttnArgs a{{*params, reinterpret_cast<const __nv_bfloat16*>(keys),
               reinterpret_cast<const __nv_bfloat16*>(values), reinterpret_cast<uint8_t*>(kv_cache),
-              block_tables, ws},
+              block_tables, reinterpret_cast<int32_t*>(workspace)},
              reinterpret_cast<const __nv_bfloat16*>(queries),
              kv_lens,
              query_start_loc,
              attention_sink,
              reinterpret_cast<__nv_bfloat16*>(out)};
-  if (launch_decode(a, (int)L.max_decode_units, sms, s) != cudaSuccess) return RPA_ERR_CUDA;
-  if (!mark(2)) return RPA_ERR_CUDA;
-  if (launch_prefill(a, (int)L.max_prefill_units, sms, s) != cudaSuccess) return RPA_ERR_CUDA;
-  if (!mark(3)) return RPA_ERR_CUDA;
-  return RPA_OK;
+  return enqueue_forward(*params, a, distribution, sms, reinterpret_cast<cudaStream_t>(stream),
+                         events);
 }
 
 extern "C" {
@@ -130,12 +136,14 @@ int rpa_update_cache(const rpa_params_t* params, const void* keys, const void* v
   if (sms <= 0) return RPA_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int32_t* ws = reinterpret_cast<int32_t*>(workspace);
-  if (launch_plan(*params, kv_lens, query_start_loc, distribution, ws, s) != cudaSuccess)
+  if (launch_plan(*params, kv_lens, query_start_loc, distribution, ws, kPrefillRows, s) !=
+      cudaSuccess)
     return RPA_ERR_CUDA;
   KvArgs a{*params, reinterpret_cast<const __nv_bfloat16*>(keys),
            reinterpret_cast<const __nv_bfloat16*>(values), reinterpret_cast<uint8_t*>(kv_cache),
            block_tables, ws};
-  if (launch_cache_write(a, kv_lens, query_start_loc, sms, s) != cudaSuccess) return RPA_ERR_CUDA;
+  if (launch_cache_write(a, kv_lens, query_start_loc, kPrefillRows, sms, s) != cudaSuccess)
+    return RPA_ERR_CUDA;
   return RPA_OK;
 }
 

@@ -35,7 +35,10 @@ struct PrefillUnit {
   int32_t seq, t_begin, t_end, head;    // new tokens [t_begin, t_end) of seq
 };
 
-constexpr int kDecodeUnitsTarget = 4096;  // planner aims for about this many splits
+#ifndef RPA_DECODE_UNITS_TARGET
+#define RPA_DECODE_UNITS_TARGET 1024
+#endif
+constexpr int kDecodeUnitsTarget = RPA_DECODE_UNITS_TARGET;  // planner aims for about this many splits
 constexpr int kDecodeChunkMin = 256;      // smallest split, in keys
 constexpr int kDecodeRows = 16;           // q-heads per decode tile (padded group)
 constexpr int kPrefillRows = 64;          // packed (token, q-head) rows per prefill tile

@@ -15,11 +15,9 @@
 #include "common.cuh"
 #include "kv_write.cuh"
 
+#include "launch.h"
+
 namespace rpa {
-cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int32_t* qsl,
-                        const int32_t* dist, int32_t* ws, cudaStream_t stream);
-cudaError_t launch_decode(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
-cudaError_t launch_prefill(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
 
 // The fixed scratch array.  Host code must not pass `g_static_workspace`
 // itself to a kernel: on the host that name is only a stand-in for the
@@ -74,20 +72,16 @@ extern "C" int rpa_forward_noalloc(const rpa_params_t* params, const void* queri
   // The planner rewrites every workspace word the kernels read (header,
   // counters of the sequences it plans, work lists), so what the previous
   // call left in the array needs no clearing.
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int32_t* w = reinterpret_cast<int32_t*>(ws);
-  const WorkspaceLayout L(*params);
-  if (launch_plan(*params, kv_lens, query_start_loc, distribution, w, s) != cudaSuccess)
-    return RPA_ERR_CUDA;
   AttnArgs a{{*params, reinterpret_cast<const __nv_bfloat16*>(keys),
               reinterpret_cast<const __nv_bfloat16*>(values),
-              reinterpret_cast<uint8_t*>(kv_cache), block_tables, w},
+              reinterpret_cast<uint8_t*>(kv_cache), block_tables, reinterpret_cast<int32_t*>(ws)},
              reinterpret_cast<const __nv_bfloat16*>(queries),
              kv_lens,
              query_start_loc,
              attention_sink,
              reinterpret_cast<__nv_bfloat16*>(out)};
-  if (launch_decode(a, (int)L.max_decode_units, sms, s) != cudaSuccess) return RPA_ERR_CUDA;
-  if (launch_prefill(a, (int)L.max_prefill_units, sms, s) != cudaSuccess) return RPA_ERR_CUDA;
+  rc = enqueue_forward(*params, a, distribution, sms, reinterpret_cast<cudaStream_t>(stream),
+                       nullptr);
+  if (rc) return rc;
   return RPA_OK;
 }

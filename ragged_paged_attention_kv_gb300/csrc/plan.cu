@@ -90,7 +90,8 @@ __device__ SeqPlan classify(const rpa_params_t& p, int s, int d0, const int32_t*
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, const int32_t* kv_lens,
                                                             const int32_t* qsl,
-                                                            const int32_t* dist, int32_t* ws) {
+                                                            const int32_t* dist, int32_t* ws,
+                                                            int prefill_rows) {
   __shared__ int s_flags;
   __shared__ int s_scan[33];
   __shared__ unsigned long long s_keys;
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   int32_t* counters = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + L.counters_off);
   const int tid = threadIdx.x;
   const int Hkv = p.num_kv_heads, G = p.num_q_heads / p.num_kv_heads;
-  const int tile_tokens = kPrefillRows / G;
+  const int tile_tokens = prefill_rows / G;  // new tokens per prefill tile
 
   if (tid == 0) {
     s_flags = 0;
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
 // Standalone page write: one warp per (token, kv head) of every planned unit.
 template <bool FP8>
 __global__ void __launch_bounds__(256) cache_write_kernel(KvArgs a, const int32_t* kv_lens,
-                                                          const int32_t* qsl) {
+                                                          const int32_t* qsl, int prefill_rows) {
   const WorkspaceLayout L(a.p);
   const DecodeUnit* dunits =
       reinterpret_cast<const DecodeUnit*>(reinterpret_cast<const char*>(a.ws) + L.decode_units_off);
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(KvArgs a, const int32_
     write_token_kv<FP8>(a, d.seq, t, kv_lens[d.seq] - 1, d.head, lane);
   }
   // prefill units: every token of the tile for the unit's head
-  const int tile_tokens = kPrefillRows / (a.p.num_q_heads / a.p.num_kv_heads);
+  const int tile_tokens = prefill_rows / (a.p.num_q_heads / a.p.num_kv_heads);
   const int64_t n_items = (int64_t)n_pf * tile_tokens;
   for (int64_t it = gw; it < n_items; it += warps) {
     const PrefillUnit pu = punits[it / tile_tokens];
@@ -241,18 +242,18 @@ __global__ void __launch_bounds__(256) cache_write_kernel(KvArgs a, const int32_
 
 // ------------------------------------------------------------ host launch
 cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int32_t* qsl,
-                        const int32_t* dist, int32_t* ws, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, kv_lens, qsl, dist, ws);
+                        const int32_t* dist, int32_t* ws, int prefill_rows, cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, kv_lens, qsl, dist, ws, prefill_rows);
   return cudaGetLastError();
 }
 
 cudaError_t launch_cache_write(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,
-                               int num_sms, cudaStream_t stream) {
+                               int prefill_rows, int num_sms, cudaStream_t stream) {
   const int grid = num_sms * 4;
   if (a.p.kv_dtype == RPA_KV_FP8_E4M3)
-    cache_write_kernel<true><<<grid, 256, 0, stream>>>(a, kv_lens, qsl);
+    cache_write_kernel<true><<<grid, 256, 0, stream>>>(a, kv_lens, qsl, prefill_rows);
   else
-    cache_write_kernel<false><<<grid, 256, 0, stream>>>(a, kv_lens, qsl);
+    cache_write_kernel<false><<<grid, 256, 0, stream>>>(a, kv_lens, qsl, prefill_rows);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,466 @@
+// Prefill / chunked-prefill path on the 5th-generation tensor cores.
+//
+// Work unit = (sequence, tile of new tokens, kv head).  The tile's 128 rows
+// are (token, q-head of the GQA group) pairs, token-major (row r is token
+// t_begin + r / G, q-head h*G + r % G), as tpu-inference RPA v3 kernel.py
+// stacks a q block's heads of one kv head, so every key/value tile serves all
+// G heads.  Per 128-key tile:
+//   S = Q K^T      tcgen05.mma, A = Q and B = K from 128-byte swizzled shared
+//                  memory, fp32 accumulator in tensor memory (two S buffers,
+//                  so the next tile's S overlaps this tile's softmax);
+//   P = softmax    one thread per row reads S from tensor memory, applies
+//                  scale / soft cap / causal + window mask, keeps the running
+//                  max m and sum l in fp32 (RPA v3
+//                  flash_attention_step1_qk_softmax), and writes P as bf16
+//                  back over S;
+//   O += P V       tcgen05.mma with A = P from tensor memory and B = V from
+//                  shared memory (RPA v3 flash_attention_step2_pv); O stays
+//                  in tensor memory and is rescaled there only when a row's
+//                  max grows by more than 2^8.
+// The RPA v3 kernel overlaps step2 of one kv head with step1 of the next;
+// here a producer warp (TMA), an MMA warp and a softmax warpgroup run
+// concurrently, synchronised by mbarriers, which overlaps the same stages.
+//
+// Keys come in two kinds of tiles: cached keys [lo, ctx) are fetched page by
+// page from the pool (one TMA box per page and 64-wide half of head_dim);
+// the step's new keys [ctx, ...) are fetched from the keys/values inputs (RPA
+// v3 _fetch_bkv does the same), in tiles aligned to ctx.  Value rows outside
+// a tile's valid range are zeroed before the PV product.  The unit's own new
+// tokens are written into their pages by the softmax warps.
+#include "async.cuh"
+#include "common.cuh"
+#include "kv_write.cuh"
+#include "tcgen05.cuh"
+#include "tma_host.h"
+
+namespace rpa {
+namespace tc {
+
+constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kM = 128;         // rows per tile
+constexpr int kN = 128;         // keys per tile
+constexpr int kD = 128;         // head_dim
+constexpr uint32_t kHalf = 128 * 128;          // [128 rows][64 bf16], 16 KB
+constexpr uint32_t kOperand = 2 * kHalf;       // [128 rows][128 bf16] as two halves
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOperand;           // key stage s at kOffK + s*kOperand
+constexpr uint32_t kOffV = 3 * kOperand;       // value stage s at kOffV + s*kOperand
+constexpr uint32_t kOffBar = 5 * kOperand;     // 160 KB
+constexpr int kSmemBytes = (int)kOffBar + 256 + 1024;
+constexpr uint32_t kTmemCols = 512;            // O [0,128), S0 [128,256), S1 [256,384)
+constexpr uint32_t kTmemO = 0, kTmemS = 128;
+constexpr int kRescaleLog2 = 8;
+
+enum Bar {
+  kBarQFull = 0,
+  kBarKFull = 1,    // [2] keys landed
+  kBarKEmpty = 3,   // [2] key stage free (S product done)
+  kBarVFull = 5,    // [2] values landed
+  kBarVReady = 7,   // [2] values fixed up, MMA may read
+  kBarVEmpty = 9,   // [2] value stage free (PV product done)
+  kBarSFull = 11,   // [2] S tile computed
+  kBarPReady = 13,  // [2] P written (and O corrected)
+  kBarPVDone = 15,  // one arrival per PV product
+  kNumBars = 16,
+};
+
+struct TcMaps {
+  CUtensorMap q;      // queries [T][Hq][D], box {64, G, 128/G}
+  CUtensorMap cache;  // pool [num_pages*P][2*Hkv][D], box {64, 1, min(P,128)}
+  CUtensorMap knew;   // keys [T][Hkv][D], box {64, 1, 128}
+  CUtensorMap vnew;   // values [T][Hkv][D], box {64, 1, 128}
+};
+
+// Geometry of one unit, computed identically by every role.
+struct UnitGeom {
+  int seq, h, q0, q_len, kv_len, ctx, t_begin, t_end;
+  int lo;              // first key any row of the tile may see
+  int c_start, n_cached, i0, n_tiles;
+  __device__ void tile(int j, bool& is_new, int& key0, int& valid) const {
+    if (j < n_cached) {
+      is_new = false;
+      key0 = c_start + kN * j;
+      valid = min(kN, ctx - key0);
+    } else {
+      is_new = true;
+      key0 = ctx + kN * (i0 + j - n_cached);
+      valid = min(kN, kv_len - key0);
+    }
+  }
+};
+
+__device__ __forceinline__ UnitGeom unit_geom(const AttnArgs& a, const PrefillUnit& pu) {
+  UnitGeom g;
+  g.seq = pu.seq;
+  g.h = pu.head;
+  g.q0 = a.qsl[pu.seq];
+  g.q_len = a.qsl[pu.seq + 1] - g.q0;
+  g.kv_len = a.kv_lens[pu.seq];
+  g.ctx = g.kv_len - g.q_len;
+  g.t_begin = pu.t_begin;
+  g.t_end = pu.t_end;
+  const int W = a.kv.p.sliding_window;
+  const int pos_first = g.ctx + g.t_begin, pos_last = g.ctx + g.t_end - 1;
+  g.lo = (W > 0 && pos_first - W + 1 > 0) ? pos_first - W + 1 : 0;
+  if (g.lo < g.ctx) {
+    g.c_start = g.lo & ~(kN - 1);
+    g.n_cached = (g.ctx - g.c_start + kN - 1) / kN;
+  } else {
+    g.c_start = 0;
+    g.n_cached = 0;
+  }
+  g.i0 = g.lo > g.ctx ? (g.lo - g.ctx) / kN : 0;
+  const int i1 = (pos_last - g.ctx) / kN;
+  g.n_tiles = g.n_cached + (i1 - g.i0 + 1);
+  return g;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ TcMaps maps, AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bars = sb + kOffBar;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_unit, s_abort;
+
+  const rpa_params_t& p = a.kv.p;
+  int32_t* hdr = a.kv.ws;
+  const WorkspaceLayout L(p);
+  const PrefillUnit* units =
+      reinterpret_cast<const PrefillUnit*>(reinterpret_cast<const char*>(hdr) + L.prefill_units_off);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  const int P = p.page_size;
+  const int W = p.sliding_window;
+  const int n_units = hdr[kHdrNumPrefill];
+
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(bar(kBarQFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarVReady + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
+      mbar_init(bar(kBarSFull + s), 1);
+      mbar_init(bar(kBarPReady + s), 4);
+    }
+    mbar_init(bar(kBarPVDone), 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&maps.q);
+    prefetch_tensormap(&maps.cache);
+    prefetch_tensormap(&maps.knew);
+    prefetch_tensormap(&maps.vnew);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  const uint32_t idesc_qk = idesc_bf16(kM, kN, false, false);
+  const uint32_t idesc_pv = idesc_bf16(kM, kD, false, true);
+  const LogitXform xf{p.softmax_scale * p.k_scale, p.logits_soft_cap,
+                      p.logits_soft_cap > 0.f ? 1.f / p.logits_soft_cap : 0.f,
+                      p.softmax_scale * p.k_scale * kLog2e};
+
+  uint32_t tcount = 0;  // tiles processed by this CTA so far (all roles agree)
+  uint32_t ucount = 0;  // units processed by this CTA so far
+  for (;;) {
+    if (tid == 0) s_unit = atomicAdd(hdr + kHdrPrefillNext, 1);
+    __syncthreads();
+    const int u = s_unit;
+    if (u >= n_units || s_abort) break;
+    const UnitGeom g = unit_geom(a, units[u]);
+    const int nt = g.n_tiles;
+
+    if (warp == 0) {
+      // ------------------------------------------------------- TMA producer
+      // Keys of tile j go into key stage j%2 once S of tile j-2 is done;
+      // values into value stage j%2 once PV of tile j-2 is done; after the
+      // values of a tile land, rows outside its valid range are zeroed.
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(kBarQFull), 2 * kHalf);
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(sb + kOffQ + hf * kHalf, &maps.q, bar(kBarQFull), hf * 64, g.h * G,
+                      g.q0 + g.t_begin);
+      }
+      // issue the boxes of one operand (kv = 0 keys, 1 values) of tile j
+      auto issue = [&](int j, int kv, uint32_t dst, uint32_t fullbar) {
+        bool is_new;
+        int key0, valid;
+        g.tile(j, is_new, key0, valid);
+        if (is_new) {
+          mbar_arrive_expect_tx(fullbar, 2 * kHalf);
+          const int row = g.q0 + (key0 - g.ctx);
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(dst + hf * kHalf, kv ? &maps.vnew : &maps.knew, fullbar, hf * 64, g.h, row);
+        } else {
+          const int rows = P < kN ? P : kN;
+          const int pg0 = key0 / P, pg1 = (key0 + valid - 1) / P;
+          mbar_arrive_expect_tx(fullbar, (uint32_t)((pg1 - pg0 + 1) * rows * 128 * 2));
+          for (int pg = pg0; pg <= pg1; ++pg) {
+            int page = __ldg(a.kv.block_tables + (int64_t)g.seq * p.pages_per_seq + pg);
+            if (page < 0 || page >= p.num_pages) {
+              set_status(hdr, RPA_STATUS_BAD_PAGE);
+              page = 0;
+            }
+            const int srow = P < kN ? pg * P - key0 : 0;
+            const int z = page * P + (P < kN ? 0 : key0 % P);
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(dst + hf * kHalf + srow * 128, &maps.cache, fullbar, hf * 64,
+                          2 * g.h + kv, z);
+          }
+        }
+      };
+      auto finalize_v = [&](uint32_t tc, int j) -> bool {
+        const int s = tc & 1;
+        if (!mbar_wait(bar(kBarVFull + s), (tc >> 1) & 1, &s_abort)) return false;
+        bool is_new;
+        int key0, valid;
+        g.tile(j, is_new, key0, valid);
+        if (valid < kN) {
+          uint8_t* v = smem + kOffV + s * kOperand;
+          for (int idx = lane; idx < (kN - valid) * 16; idx += 32) {
+            const int r = valid + idx / 16, c = idx % 16;  // 16 chunks over both halves
+            *reinterpret_cast<uint4*>(v + (c >> 3) * kHalf + r * 128 + (c & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarVReady + s));
+        return true;
+      };
+      bool ok = true;
+      for (int j = 0; j < nt && ok; ++j) {
+        const uint32_t tc = tcount + j;
+        const int s = tc & 1;
+        const uint32_t par = ((tc >> 1) & 1) ^ 1;
+        if (!mbar_wait(bar(kBarKEmpty + s), par, &s_abort)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) issue(j, 0, sb + kOffK + s * kOperand, bar(kBarKFull + s));
+        if (!mbar_wait(bar(kBarVEmpty + s), par, &s_abort)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) issue(j, 1, sb + kOffV + s * kOperand, bar(kBarVFull + s));
+        __syncwarp();
+        if (j >= 1) ok = finalize_v(tc - 1, j - 1);
+      }
+      if (ok && nt >= 1) ok = finalize_v(tcount + nt - 1, nt - 1);
+      if (!ok && lane == 0) {
+        set_status(hdr, RPA_STATUS_TIMEOUT);
+        s_abort = 1;
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA
+      // Order: S(0), then for each tile j: S(j+1), PV(j) -- the next tile's
+      // scores are computed while the softmax warps work on tile j.
+      if (lane == 0) {
+        bool ok = mbar_wait(bar(kBarQFull), ucount & 1, &s_abort);
+        tc_fence_after();
+        auto qk = [&](uint32_t tc) -> bool {
+          const int s = tc & 1;
+          if (!mbar_wait(bar(kBarKFull + s), (tc >> 1) & 1, &s_abort)) return false;
+          tc_fence_after();
+          const uint32_t sK = sb + kOffK + s * kOperand;
+          for (int k = 0; k < kD / 16; ++k) {
+            const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+            umma_ss(tmem + kTmemS + 128 * s, sdesc_sw128(sb + kOffQ + off, 16, 1024),
+                    sdesc_sw128(sK + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(kBarKEmpty + s));
+          umma_commit(bar(kBarSFull + s));
+          return true;
+        };
+        auto pv = [&](uint32_t tc, int j) -> bool {
+          const int s = tc & 1;
+          if (!mbar_wait(bar(kBarPReady + s), (tc >> 1) & 1, &s_abort)) return false;
+          if (!mbar_wait(bar(kBarVReady + s), (tc >> 1) & 1, &s_abort)) return false;
+          tc_fence_after();
+          const uint32_t sV = sb + kOffV + s * kOperand;
+          for (int k = 0; k < kN / 16; ++k) {
+            const uint64_t bd = sdesc_sw128(sV + k * 16 * 128, kHalf, 1024);
+            umma_ts(tmem + kTmemO, tmem + kTmemS + 128 * s + 8 * k, bd, idesc_pv,
+                    (j > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(kBarVEmpty + s));
+          umma_commit(bar(kBarPVDone));
+          return true;
+        };
+        if (ok && nt >= 1) ok = qk(tcount);
+        for (int j = 0; j < nt && ok; ++j) {
+          if (j + 1 < nt) ok = qk(tcount + j + 1);
+          if (ok) ok = pv(tcount + j, j);
+        }
+        if (!ok) {
+          set_status(hdr, RPA_STATUS_TIMEOUT);
+          s_abort = 1;
+        }
+      }
+    } else {
+      // --------------------------------------------------- softmax warps
+      const int q4 = warp & 3;                 // tensor-memory lane quarter
+      const int r = 32 * q4 + lane;            // row of the tile
+      const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+      const int ti = r / G;
+      const bool row_valid = g.t_begin + ti < g.t_end;
+      const int i_tok = g.t_begin + min(ti, g.t_end - g.t_begin - 1);
+      const int pos = g.ctx + i_tok;
+      const int hq = g.h * G + r % G;
+
+      // this unit's new tokens -> their pages (one warp per token)
+      for (int i = warp - 2; i < g.t_end - g.t_begin; i += 4)
+        write_token_kv<false>(a.kv, g.seq, g.q0 + g.t_begin + i, g.ctx + g.t_begin + i, g.h, lane);
+
+      float m_run = a.sink ? a.sink[hq] * kLog2e : -INFINITY;
+      float l_run = a.sink ? 1.f : 0.f;
+      bool ok = true;
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t tc = tcount + j;
+        const int s = tc & 1;
+        if (!mbar_wait(bar(kBarSFull + s), (tc >> 1) & 1, &s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        bool is_new;
+        int key0, valid;
+        g.tile(j, is_new, key0, valid);
+        uint32_t sr[128];
+        tmem_ld128(tmem + lane_off + kTmemS + 128 * s, sr);
+        const bool full = valid == kN && key0 + kN - 1 <= pos && (W == 0 || pos - key0 < W);
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kN; ++c) {
+          float x = xf(__uint_as_float(sr[c]));
+          if (!full) {
+            const int jk = key0 + c;
+            const bool okk = c < valid && jk <= pos && (W == 0 || pos - jk < W);
+            x = okk ? x : -INFINITY;
+          }
+          sr[c] = __float_as_uint(x);
+          mt = fmaxf(mt, x);
+        }
+        // lazy rescale: move the max only when it grows by more than 2^8
+        const bool need = mt > m_run + (float)kRescaleLog2;
+        float alpha = 1.f;
+        if (need) {
+          alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - mt);
+          m_run = mt;
+          l_run *= alpha;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O must hold P V of every earlier tile before it is rescaled
+          if (!mbar_wait(bar(kBarPVDone), (tc - 1) & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < kD; c0 += 32) {
+            uint32_t oc[32];
+            tmem_ld32(tmem + lane_off + kTmemO + c0, oc);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) oc[c] = __float_as_uint(__uint_as_float(oc[c]) * alpha);
+            tmem_st32p(tmem + lane_off + kTmemO + c0, oc);
+          }
+        }
+        const float msafe = m_run == -INFINITY ? 0.f : m_run;
+        float rs = 0.f;
+        // P packed as bf16 pairs into sr[0..64): sr[c/2] is already consumed
+#pragma unroll
+        for (int c = 0; c < kN; c += 2) {
+          const float p0 = exp2f(__uint_as_float(sr[c]) - msafe);
+          const float p1 = exp2f(__uint_as_float(sr[c + 1]) - msafe);
+          rs += p0 + p1;
+          sr[c >> 1] = pack_bf16(p0, p1);
+        }
+        l_run += rs;
+        tmem_st64p(tmem + lane_off + kTmemS + 128 * s, sr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPReady + s));
+      }
+      // epilogue: O / l -> bf16 rows
+      if (ok && nt >= 1) {
+        if (!mbar_wait(bar(kBarPVDone), (tcount + nt - 1) & 1, &s_abort)) ok = false;
+      }
+      if (ok) {
+        tc_fence_after();
+        uint32_t orow[128];
+        tmem_ld128(tmem + lane_off + kTmemO, orow);
+        if (row_valid) {
+          const float inv = p.v_scale / l_run;
+          __nv_bfloat16* dst = a.out + ((int64_t)(g.q0 + g.t_begin + ti) * p.num_q_heads + hq) * kD;
+#pragma unroll
+          for (int c = 0; c < kD; c += 8) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(orow[c + 4]) * inv, __uint_as_float(orow[c + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(orow[c + 6]) * inv, __uint_as_float(orow[c + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c) = v;
+          }
+        }
+      } else if (lane == 0) {
+        set_status(hdr, RPA_STATUS_TIMEOUT);
+        s_abort = 1;
+      }
+    }
+    tcount += nt;
+    ucount += 1;
+    tc_fence_before();
+    __syncthreads();  // the next unit reuses Q, the stages and tensor memory
+    tc_fence_after();
+  }
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace tc
+
+bool prefill_uses_tc(const rpa_params_t& p) {
+  const int G = p.num_q_heads / p.num_kv_heads;
+  return p.head_dim == 128 && p.kv_dtype == RPA_KV_BF16 && p.page_size >= 8 && G >= 1 && G <= 16;
+}
+
+cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream) {
+  static std::atomic<unsigned long long> attr_done{0};
+  auto kern = tc::prefill_tc_kernel;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), tc::kSmemBytes, &attr_done);
+  if (e != cudaSuccess) return e;
+  const rpa_params_t& p = a.kv.p;
+  const int G = p.num_q_heads / p.num_kv_heads;
+  tc::TcMaps maps;
+  const uint64_t T = (uint64_t)(p.total_tokens > 0 ? p.total_tokens : 1);
+  const uint32_t prow = p.page_size < tc::kN ? (uint32_t)p.page_size : (uint32_t)tc::kN;
+  bool ok = encode_map_3d(&maps.q, a.queries, 2, 128, (uint64_t)p.num_q_heads, T, 64u,
+                          (uint32_t)G, (uint32_t)(tc::kM / G), true) &&
+            encode_map_3d(&maps.cache, a.kv.cache, 2, 128, 2 * (uint64_t)p.num_kv_heads,
+                          (uint64_t)p.num_pages * p.page_size, 64u, 1u, prow, true) &&
+            encode_map_3d(&maps.knew, a.kv.keys, 2, 128, (uint64_t)p.num_kv_heads, T, 64u, 1u,
+                          128u, true) &&
+            encode_map_3d(&maps.vnew, a.kv.values, 2, 128, (uint64_t)p.num_kv_heads, T, 64u, 1u,
+                          128u, true);
+  if (!ok) return cudaErrorInvalidValue;
+  int grid = num_sms;
+  if (grid > max_units) grid = max_units;
+  if (grid < 1) grid = 1;
+  kern<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(maps, a);
+  return cudaGetLastError();
+}
+
+}  // namespace rpa
