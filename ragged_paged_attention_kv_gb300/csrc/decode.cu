@@ -38,9 +38,10 @@ template <int D, bool FP8>
 struct Cfg {
   static constexpr int kRowBytes = FP8 ? D : 128;        // bytes of one box row in smem
   static constexpr int kHalves = FP8 ? 1 : D / 64;       // boxes across head_dim
-  static constexpr int kHalfBytes = kBN * kRowBytes;
-  static constexpr int kKVBytes = kHalves * kHalfBytes;  // keys (or values) of one stage
-  static constexpr int kStageBytes = 2 * kKVBytes;
+  // a stage holds, per 64-wide half of head_dim, 2*kBN rows: key j at row 2j,
+  // value j at row 2j+1 (one TMA box brings both for a page)
+  static constexpr int kHalfBytes = 2 * kBN * kRowBytes;
+  static constexpr int kStageBytes = kHalves * kHalfBytes;
   static constexpr int kQBytes = kDecodeRows * D * 2;    // one query slot
   static constexpr int kConvBytes = FP8 ? kConsumerWarps * 2 * kKeysPerWarp * D * 2 : 0;
   static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * (D + 2) * 4;
@@ -69,11 +70,10 @@ struct DecodeMaps {
   CUtensorMap cache;  // pool [num_pages*P][2*Hkv][D]
 };
 
-// Address of 16-byte chunk `c` (of D/8) of key row `r` in a bf16 stage tile
-// written by 128-byte swizzled boxes (one box per 64-wide half).
-template <int D>
-__device__ __forceinline__ uint32_t stage_addr(uint32_t tile, int r, int c) {
-  return tile + (uint32_t)((c >> 3) * kBN * 128) + sw128(r, c & 7);
+// Address of 16-byte chunk `c` (of D/8) of the key (kv = 0) or value (kv = 1)
+// row of key `r` in a bf16 stage written by 128-byte swizzled boxes.
+__device__ __forceinline__ uint32_t kv_addr(uint32_t stage, int r, int kv, int c) {
+  return stage + (uint32_t)((c >> 3) * 2 * kBN * 128) + sw128(2 * r + kv, c & 7);
 }
 
 template <int D, bool FP8>
@@ -215,10 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int row_in_stage = P < kBN ? (pg0 + k) * P - kb : 0;
           const int z = page * P + (P < kBN ? 0 : kb % P);
-          for (int kv = 0; kv < 2; ++kv)
-            for (int hf = 0; hf < C::kHalves; ++hf)
-              tma_load_3d(stage + kv * C::kKVBytes + hf * C::kHalfBytes + row_in_stage * C::kRowBytes,
-                          &maps.cache, bar_full + 8 * s, FP8 ? 0 : hf * 64, 2 * du.head + kv, z);
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(stage + hf * C::kHalfBytes + 2 * row_in_stage * C::kRowBytes, &maps.cache,
+                        bar_full + 8 * s, FP8 ? 0 : hf * 64, 2 * du.head, z);
         }
       }
     }
@@ -303,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      kv ? p.v_scale : p.k_scale));
           } else {
             const uint2 codes = *reinterpret_cast<const uint2*>(
-                smem + (stage - s_base) + kv * C::kKVBytes + (warp * kKeysPerWarp + r) * C::kRowBytes + c * 8);
+                smem + (stage - s_base) + (2 * (warp * kKeysPerWarp + r) + kv) * C::kRowBytes + c * 8);
             val = dequant8(codes);
           }
           *reinterpret_cast<uint4*>((kv ? gV : gK) + swz(r, c, D * 2)) = val;
@@ -313,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tV = cV;
         krow0 = 0;
       } else {
-        tK = stage;
-        tV = stage + C::kKVBytes;
+        tK = stage;  // keys and values interleaved: see kv_addr
+        tV = stage;
         krow0 = warp * kKeysPerWarp;
         // rows outside [k_begin, k_end): zero the values (masked keys may hold
         // anything, and 0 * NaN would poison P V); the new token's row: inputs
@@ -325,13 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = idx / (D / 8), c = idx % (D / 8);
             const int j = kw + r;
             if (j < du.k_begin || j >= du.k_end) {
-              *reinterpret_cast<uint4*>(smem + (stage_addr<D>(tV, krow0 + r, c) - s_base)) =
+              *reinterpret_cast<uint4*>(smem + (kv_addr(stage, krow0 + r, 1, c) - s_base)) =
                   make_uint4(0, 0, 0, 0);
             } else if (j == ctx) {
               const int64_t off = ((int64_t)q0 * p.num_kv_heads + h) * D + c * 8;
-              *reinterpret_cast<uint4*>(smem + (stage_addr<D>(tK, krow0 + r, c) - s_base)) =
+              *reinterpret_cast<uint4*>(smem + (kv_addr(stage, krow0 + r, 0, c) - s_base)) =
                   __ldg(reinterpret_cast<const uint4*>(a.kv.keys + off));
-              *reinterpret_cast<uint4*>(smem + (stage_addr<D>(tV, krow0 + r, c) - s_base)) =
+              *reinterpret_cast<uint4*>(smem + (kv_addr(stage, krow0 + r, 1, c) - s_base)) =
                   __ldg(reinterpret_cast<const uint4*>(a.kv.values + off));
             }
           }
@@ -349,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mi = lane >> 3;
         const int key = krow0 + (lane & 7) + ((mi >> 1) << 3);
         const int chunk = 2 * ks + (mi & 1);
-        const uint32_t addr = FP8 ? tK + swz(key, chunk, D * 2) : stage_addr<D>(tK, key, chunk);
+        const uint32_t addr = FP8 ? tK + swz(key, chunk, D * 2) : kv_addr(tK, key, 0, chunk);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(addr, b0, b1, b2, b3);
         mma_bf16_16816(sc[0], qa[ks], b0, b1);
@@ -410,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mi = lane >> 3;
         const int key = krow0 + (lane & 7) + ((mi & 1) << 3);
         const int chunk = 2 * cp + (mi >> 1);
-        const uint32_t addr = FP8 ? tV + swz(key, chunk, D * 2) : stage_addr<D>(tV, key, chunk);
+        const uint32_t addr = FP8 ? tV + swz(key, chunk, D * 2) : kv_addr(tV, key, 1, chunk);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(addr, b0, b1, b2, b3);
         mma_bf16_16816(o[2 * cp], pa, b0, b1);
@@ -550,7 +549,7 @@ static cudaError_t launch_decode_t(const AttnArgs& a, int max_units, int num_sms
   const uint32_t rows = p.page_size < dec::kBN ? (uint32_t)p.page_size : (uint32_t)dec::kBN;
   if (!encode_map_3d(&maps.cache, a.kv.cache, FP8 ? 1 : 2, (uint64_t)D,
                      2 * (uint64_t)p.num_kv_heads, (uint64_t)p.num_pages * p.page_size,
-                     FP8 ? (uint32_t)D : 64u, 1u, rows, !FP8))
+                     FP8 ? (uint32_t)D : 64u, 2u, rows, !FP8))
     return cudaErrorInvalidValue;
   int grid = num_sms;
   if (grid > max_units) grid = max_units;
