@@ -52,6 +52,8 @@ DESCRIPTIONS = {
            "(kv~U[256,16384]) + 8x256 chunks (prior kv~U[0,8192]); Hq64/Hkv8/D64, page_size 16",
     "decode_small": "decode shape at 64 seqs (profiling size): q_len=1, kv_len~U[512,4096]; "
                     "Hq32/Hkv8/D128, bf16, page_size 16, pool = pages used + 10%",
+    "long_small": "long-context shape at profiling size: 1 seq q=kv=8192 causal; Hq32/Hkv8/D128, "
+                  "bf16, page_size 64",
     "tiny": "tiny mixed batch: 3 seqs (1,17),(24,24),(5,40); Hq4/Hkv2/D64/P16",
 }
 

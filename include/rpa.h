@@ -100,7 +100,7 @@ typedef struct {
   int32_t total_tokens;   /* T: rows of queries/keys/values/out             */
   int32_t kv_dtype;       /* rpa_kv_dtype_t                                 */
   int32_t sliding_window; /* W > 0 keeps p - j < W; 0 = no window           */
-  float softmax_scale;    /* applied to q.k as given                        */
+  float softmax_scale;    /* > 0; applied to q.k as given                   */
   float logits_soft_cap;  /* > 0 enables cap*tanh(x/cap); 0 = none          */
   float k_scale;          /* fp8: dequantisation scales; bf16: must be 1    */
   float v_scale;

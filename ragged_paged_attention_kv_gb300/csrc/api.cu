@@ -28,7 +28,7 @@ static int check_params(const rpa_params_t* p) {
   // fp8 rows of 64 bytes need at least two rows per page for 128-byte aligned copies
   if (p->kv_dtype == RPA_KV_FP8_E4M3 && p->head_dim == 64 && p->page_size < 2)
     return RPA_ERR_UNSUPPORTED;
-  if (!(p->softmax_scale == p->softmax_scale) || !(p->logits_soft_cap >= 0.f))
+  if (!(p->softmax_scale > 0.f) || !(p->logits_soft_cap >= 0.f))
     return RPA_ERR_INVALID_ARG;
   if (p->kv_dtype == RPA_KV_FP8_E4M3) {
     if (!(p->k_scale > 0.f) || !(p->v_scale > 0.f)) return RPA_ERR_INVALID_ARG;

@@ -179,6 +179,14 @@ __device__ __forceinline__ float quad_sum(float x) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// 2^x with the hardware approximation (one MUFU operation; denormal results
+// flush to zero, which only affects weights below 2^-126).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Logit transform shared by the kernels: raw dot product -> log2-domain
 // logit.  scale_log2 = softmax_scale * k_scale * log2(e); with a soft cap,
 // cap * tanh(x / cap) is applied to the natural-domain logit first.

@@ -61,7 +61,8 @@ enum Bar {
   kBarSFull = 11,   // [2] S tile computed
   kBarPReady = 13,  // [2] P written (and O corrected)
   kBarPVDone = 15,  // one arrival per PV product
-  kNumBars = 16,
+  kBarODone = 16,   // one arrival per unit, after its last PV product
+  kNumBars = 17,
 };
 
 struct TcMaps {
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarPReady + s), 4);
     }
     mbar_init(bar(kBarPVDone), 1);
+    mbar_init(bar(kBarODone), 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -172,6 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const LogitXform xf{p.softmax_scale * p.k_scale, p.logits_soft_cap,
                       p.logits_soft_cap > 0.f ? 1.f / p.logits_soft_cap : 0.f,
                       p.softmax_scale * p.k_scale * kLog2e};
+  const bool has_cap = p.logits_soft_cap > 0.f;
+  const float sc = has_cap ? 1.f : xf.scale_log2;  // raw score -> log2-domain logit
 
   uint32_t tcount = 0;  // tiles processed by this CTA so far (all roles agree)
   uint32_t ucount = 0;  // units processed by this CTA so far
@@ -305,6 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j + 1 < nt) ok = qk(tcount + j + 1);
           if (ok) ok = pv(tcount + j, j);
         }
+        // A parity wait only tells the current phase from the previous one,
+        // so the epilogue, which may be two PV products ahead of PVDone,
+        // waits on this once-per-unit barrier instead.
+        if (ok) umma_commit(bar(kBarODone));
         if (!ok) {
           set_status(hdr, RPA_STATUS_TIMEOUT);
           s_abort = 1;
@@ -342,18 +350,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[128];
         tmem_ld128(tmem + lane_off + kTmemS + 128 * s, sr);
         const bool full = valid == kN && key0 + kN - 1 <= pos && (W == 0 || pos - key0 < W);
-        float mt = -INFINITY;
+        // logits in the log2 domain are fma(s, sc, -m): with a soft cap the
+        // capped logit is formed first and sc is 1
+        if (has_cap) {
 #pragma unroll
-        for (int c = 0; c < kN; ++c) {
-          float x = xf(__uint_as_float(sr[c]));
-          if (!full) {
+          for (int c = 0; c < kN; ++c) sr[c] = __float_as_uint(xf(__uint_as_float(sr[c])));
+        }
+        if (!full) {
+#pragma unroll
+          for (int c = 0; c < kN; ++c) {
             const int jk = key0 + c;
             const bool okk = c < valid && jk <= pos && (W == 0 || pos - jk < W);
-            x = okk ? x : -INFINITY;
+            if (!okk) sr[c] = __float_as_uint(-INFINITY);
           }
-          sr[c] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
         }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kN; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c]));
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
         // lazy rescale: move the max only when it grows by more than 2^8
         const bool need = mt > m_run + (float)kRescaleLog2;
         float alpha = 1.f;
@@ -363,7 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= alpha;
         }
         if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // O must hold P V of every earlier tile before it is rescaled
+          // O must hold P V of every earlier tile before it is rescaled.  The
+          // parity wait is exact here: S of this tile was committed after PV of
+          // tile tc-2, and PV of this tile needs our P, so PVDone has completed
+          // either tc-1 or tc phases.
           if (!mbar_wait(bar(kBarPVDone), (tc - 1) & 1, &s_abort)) {
             ok = false;
             break;
@@ -378,26 +395,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32p(tmem + lane_off + kTmemO + c0, oc);
           }
         }
-        const float msafe = m_run == -INFINITY ? 0.f : m_run;
-        float rs = 0.f;
+        const float nm = m_run == -INFINITY ? 0.f : -m_run;
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
         // P packed as bf16 pairs into sr[0..64): sr[c/2] is already consumed
 #pragma unroll
         for (int c = 0; c < kN; c += 2) {
-          const float p0 = exp2f(__uint_as_float(sr[c]) - msafe);
-          const float p1 = exp2f(__uint_as_float(sr[c + 1]) - msafe);
-          rs += p0 + p1;
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sc, nm));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sc, nm));
+          rs[(c >> 1) & 3] += p0 + p1;
           sr[c >> 1] = pack_bf16(p0, p1);
         }
-        l_run += rs;
+        l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
         tmem_st64p(tmem + lane_off + kTmemS + 128 * s, sr);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarPReady + s));
       }
       // epilogue: O / l -> bf16 rows
-      if (ok && nt >= 1) {
-        if (!mbar_wait(bar(kBarPVDone), (tcount + nt - 1) & 1, &s_abort)) ok = false;
-      }
+      if (ok && !mbar_wait(bar(kBarODone), ucount & 1, &s_abort)) ok = false;
       if (ok) {
         tc_fence_after();
         uint32_t orow[128];

@@ -362,6 +362,23 @@ def long(sliding_window: int = 0) -> Workload:
                     distribution=np.array([0, 0, 2], np.int32), total_tokens=2 * L)
 
 
+def long_small() -> Workload:
+    """The long-context shape at one sequence of 8192 tokens (profiling size)."""
+    seed = 1014
+    g = torch.Generator().manual_seed(seed)
+    P, L = 64, 8192
+    q = np.full(1, L, np.int32)
+    kv = np.full(1, L, np.int32)
+    pps = L // P
+    bt = _assign_pages(kv, P, 256, 1, pps, g)
+    return Workload(name="long_small", seed=seed, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                    page_size=P, num_pages=256, pages_per_seq=pps, max_num_seqs=1,
+                    kv_dtype="bf16", softmax_scale=1.0 / math.sqrt(128), sliding_window=0,
+                    logits_soft_cap=0.0, k_scale=1.0, v_scale=1.0, has_sink=False,
+                    q_lens=q, kv_lens_valid=kv, block_tables=bt,
+                    distribution=np.array([0, 0, 1], np.int32), total_tokens=L)
+
+
 def fp8() -> Workload:
     seed = 1005
     g = torch.Generator().manual_seed(seed)
@@ -390,6 +407,7 @@ WORKLOADS = {
     "mixed": mixed,
     "long": lambda: long(0),
     "long_w4096": lambda: long(4096),
+    "long_small": long_small,
     "fp8": fp8,
 }
 

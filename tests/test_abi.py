@@ -68,6 +68,8 @@ def test_workspace_size_host_only(lib):
     (dict(k_scale=0.5), 1),              # bf16 cache needs unit scales
     (dict(kv_fp8=True, k_scale=0.0), 1),
     (dict(logits_soft_cap=-1.0), 1),
+    (dict(softmax_scale=0.0), 1),
+    (dict(softmax_scale=-0.5), 1),
 ])
 def test_invalid_params_are_refused(lib, over, code):
     n = ctypes.c_size_t(0)

@@ -142,6 +142,24 @@ def test_distribution_only_selects_tiles():
         assert np.mean(np.abs(o - outs[0])) <= 2e-3
 
 
+def test_repeated_calls_match_oracle_every_time():
+    """Short units with cached and new key tiles, run repeatedly on fresh
+    workspaces: a pipeline race shows up as an occasional wrong call."""
+    w = _case("rr", 125, [1] * 10 + [70, 33],
+              [1500, 40, 900, 2200, 1, 300, 1023, 64, 777, 2048, 300, 33],
+              num_q_heads=32, num_kv_heads=8, head_dim=128, has_sink=True)
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu")
+    sink = w.make_sink()
+    ref, ref_cache = run_oracle(w, q, k, v, pool, sink)
+    n = w.num_query_tokens
+    for it in range(10):
+        out, pool_after, status = run_gpu(w, q, k, v, pool, sink)
+        assert status == 0
+        assert np.array_equal(pool_bytes(pool_after), ref_cache)
+        assert_close(out[:n], ref, f"call {it}")
+
+
 def test_decode_class_with_long_query_is_flagged_and_computed():
     w = _case("dq", 123, [1, 3, 1], [30, 10, 5], distribution=[3, 3, 3])
     check_case(w, expect_status=oracle_status_decode_qlen())
