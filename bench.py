@@ -170,6 +170,18 @@ def load_peaks():
                 "source": "fallback"}
 
 
+def kernel_source_sha(kernel_file: str) -> str:
+    """Hash of a kernel's translation unit and every shared header."""
+    import glob
+    csrc = os.path.join(ROOT, "ragged_paged_attention_kv_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in [os.path.join(csrc, kernel_file)] + sorted(glob.glob(os.path.join(csrc, "*.cuh"))) + \
+            sorted(glob.glob(os.path.join(csrc, "*.h"))) + [os.path.join(ROOT, "include", "rpa.h")]:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel_file: str, workload: str):
     """DRAM bytes per launch from a committed ncu capture, if the kernel's
     source is unchanged since the capture; else None."""
@@ -178,9 +190,7 @@ def traffic_for(kernel_file: str, workload: str):
         with open(path) as f:
             table = json.load(f)
         ent = table[workload]
-        src = os.path.join(ROOT, "ragged_paged_attention_kv_gb300", "csrc", ent["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if sha != ent["source_sha"] or ent["source"] != kernel_file:
+        if ent["source"] != kernel_file or kernel_source_sha(kernel_file) != ent["source_sha"]:
             return None
         return float(ent["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
