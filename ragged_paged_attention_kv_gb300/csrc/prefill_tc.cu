@@ -198,27 +198,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sb + kOffQ + hf * kHalf, &maps.q, bar(kBarQFull), hf * 64, g.h * G,
                       g.q0 + g.t_begin);
       }
-      // issue the boxes of one operand (kv = 0 keys, 1 values) of tile j
-      auto issue = [&](int j, int kv, uint32_t dst, uint32_t fullbar) {
+      // Page ids of a cached tile: lane l holds page pg0 + l (a tile spans at
+      // most 128/P + 1 <= 17 pages for P >= 8), loaded one tile ahead so the
+      // block-table reads overlap the wait for a free stage.
+      const int64_t bt_row = (int64_t)g.seq * p.pages_per_seq;
+      auto load_ids = [&](int j) -> int {
+        bool is_new;
+        int key0, valid;
+        g.tile(j, is_new, key0, valid);
+        if (is_new) return 0;
+        const int pg0 = key0 / P, npg = (key0 + valid - 1) / P - pg0 + 1;
+        return lane < npg ? __ldg(a.kv.block_tables + bt_row + pg0 + lane) : 0;
+      };
+      // issue the boxes of one operand (kv = 0 keys, 1 values) of tile j; each
+      // lane copies its own page
+      auto issue = [&](int j, int kv, uint32_t dst, uint32_t fullbar, int page) {
         bool is_new;
         int key0, valid;
         g.tile(j, is_new, key0, valid);
         if (is_new) {
-          mbar_arrive_expect_tx(fullbar, 2 * kHalf);
-          const int row = g.q0 + (key0 - g.ctx);
-          for (int hf = 0; hf < 2; ++hf)
-            tma_load_3d(dst + hf * kHalf, kv ? &maps.vnew : &maps.knew, fullbar, hf * 64, g.h, row);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fullbar, 2 * kHalf);
+            const int row = g.q0 + (key0 - g.ctx);
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(dst + hf * kHalf, kv ? &maps.vnew : &maps.knew, fullbar, hf * 64, g.h,
+                          row);
+          }
         } else {
           const int rows = P < kN ? P : kN;
-          const int pg0 = key0 / P, pg1 = (key0 + valid - 1) / P;
-          mbar_arrive_expect_tx(fullbar, (uint32_t)((pg1 - pg0 + 1) * rows * 128 * 2));
-          for (int pg = pg0; pg <= pg1; ++pg) {
-            int page = __ldg(a.kv.block_tables + (int64_t)g.seq * p.pages_per_seq + pg);
+          const int pg0 = key0 / P, npg = (key0 + valid - 1) / P - pg0 + 1;
+          if (lane == 0) mbar_arrive_expect_tx(fullbar, (uint32_t)(npg * rows * 128 * 2));
+          __syncwarp();
+          if (lane < npg) {
             if (page < 0 || page >= p.num_pages) {
               set_status(hdr, RPA_STATUS_BAD_PAGE);
               page = 0;
             }
-            const int srow = P < kN ? pg * P - key0 : 0;
+            const int srow = P < kN ? (pg0 + lane) * P - key0 : 0;
             const int z = page * P + (P < kN ? 0 : key0 % P);
             for (int hf = 0; hf < 2; ++hf)
               tma_load_3d(dst + hf * kHalf + srow * 128, &maps.cache, fullbar, hf * 64,
@@ -246,20 +262,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       bool ok = true;
+      int ids_next = load_ids(0);
       for (int j = 0; j < nt && ok; ++j) {
         const uint32_t tc = tcount + j;
         const int s = tc & 1;
         const uint32_t par = ((tc >> 1) & 1) ^ 1;
+        const int ids = ids_next;
+        if (j + 1 < nt) ids_next = load_ids(j + 1);
         if (!mbar_wait(bar(kBarKEmpty + s), par, &s_abort)) {
           ok = false;
           break;
         }
-        if (lane == 0) issue(j, 0, sb + kOffK + s * kOperand, bar(kBarKFull + s));
+        issue(j, 0, sb + kOffK + s * kOperand, bar(kBarKFull + s), ids);
         if (!mbar_wait(bar(kBarVEmpty + s), par, &s_abort)) {
           ok = false;
           break;
         }
-        if (lane == 0) issue(j, 1, sb + kOffV + s * kOperand, bar(kBarVFull + s));
+        issue(j, 1, sb + kOffV + s * kOperand, bar(kBarVFull + s), ids);
         __syncwarp();
         if (j >= 1) ok = finalize_v(tc - 1, j - 1);
       }
