@@ -120,6 +120,37 @@ def test_small_cases(name, make):
     check_case(make())
 
 
+def _tc(name, seed, q_lens, kv_lens, **kw):
+    """A case that takes the tcgen05 prefill path (bf16 cache, head_dim 128, P >= 8)."""
+    base = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    base.update(kw)
+    return wl.make_custom(name, seed, q_lens, kv_lens, **base)
+
+
+TC_CASES = [
+    ("p8", lambda: _tc("t8", 201, [1, 90, 13], [70, 400, 141], page_size=8)),
+    ("p128", lambda: _tc("t128", 202, [1, 200, 7], [900, 700, 135], page_size=128)),
+    ("p256_partial_pages", lambda: _tc("t256", 203, [150, 40], [1000, 40], page_size=256)),
+    ("p1024", lambda: _tc("t1k", 204, [1, 130], [1500, 1200], page_size=1024)),
+    ("gqa1_long_tiles", lambda: _tc("tg1", 205, [300, 129, 1], [900, 129, 50], num_q_heads=4,
+                                    num_kv_heads=4)),
+    ("gqa16", lambda: _tc("tg16", 206, [1, 37, 9], [260, 300, 9], num_q_heads=32,
+                          num_kv_heads=2)),
+    ("window_in_cached_tiles", lambda: _tc("tw", 207, [1, 100, 64], [2000, 1500, 64],
+                                           sliding_window=200)),
+    ("window_short", lambda: _tc("tws", 208, [70, 1], [600, 333], sliding_window=5)),
+    ("softcap_sink", lambda: _tc("tcs", 209, [1, 90, 33], [500, 300, 33], logits_soft_cap=7.5,
+                                 has_sink=True, softmax_scale=0.2)),
+    ("ctx_tile_aligned", lambda: _tc("tca", 210, [128, 1], [384, 129], page_size=32)),
+    ("many_tiles_ragged", lambda: _tc("tmr", 211, [517, 3, 1], [1800, 700, 60], page_size=64)),
+]
+
+
+@pytest.mark.parametrize("name,make", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_tcgen05_prefill_cases(name, make):
+    check_case(make())
+
+
 def test_decode_split_boundaries():
     # kv lengths at page and split boundaries, all decode, big enough batch that
     # the planner's split size stays at its minimum
