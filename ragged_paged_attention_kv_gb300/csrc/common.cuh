@@ -139,17 +139,29 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
   return pack_bf16(f.x, f.y);
 }
 
+// x / s (s > 0) rounded to nearest fp32, from r = RN(1/s): q = RN(x*r), then
+// one residual correction q + (x - s*q)*r with fused multiply-adds.  With a
+// correctly rounded reciprocal this is the correctly rounded quotient
+// (Markstein's theorem) away from overflow and subnormal quotients; both of
+// those encode to the same e4m3 code either way (saturation, or +-0).  The
+// correction turns -0 into +0, so the sign is taken from x.
+__device__ __forceinline__ float div_by(float x, float s, float r) {
+  const float q = x * r;
+  return copysignf(fmaf(fmaf(-q, s, x), r, q), x);
+}
+
 // Quantise 8 bf16 values (one 16-byte chunk) to 8 e4m3 codes: x / scale in
-// fp32 with an IEEE divide, then e4m3.  Returns the 8 codes as a uint2.
+// fp32, correctly rounded, then e4m3.  Returns the 8 codes as a uint2.
 __device__ __forceinline__ uint2 quantize8(uint4 src, float scale) {
   const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&src);
+  const float r = __frcp_rn(scale);
   uint32_t w[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     float2 a = __bfloat1622float2(b[2 * i]);
     float2 c = __bfloat1622float2(b[2 * i + 1]);
-    uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(a.x, scale), __fdiv_rn(a.y, scale));
-    uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(c.x, scale), __fdiv_rn(c.y, scale));
+    uint32_t lo = f32x2_to_e4m3x2(div_by(a.x, scale, r), div_by(a.y, scale, r));
+    uint32_t hi = f32x2_to_e4m3x2(div_by(c.x, scale, r), div_by(c.y, scale, r));
     w[i] = lo | (hi << 16);
   }
   return make_uint2(w[0], w[1]);
@@ -187,6 +199,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// tanh(x) = 1 - 2 / (e^(2x) + 1), with the hardware 2^x and reciprocal
+// approximations: absolute error of a few 1e-7, and exactly +-1 in the
+// limits (e^(2x) = inf gives a reciprocal of 0, e^(2x) = 0 gives 1).
+__device__ __forceinline__ float tanh_exp(float x) {
+  const float e = fast_exp2(x * (2.f * kLog2e));
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(e + 1.f));
+  return fmaf(-2.f, r, 1.f);
+}
+
 // Logit transform shared by the kernels: raw dot product -> log2-domain
 // logit.  scale_log2 = softmax_scale * k_scale * log2(e); with a soft cap,
 // cap * tanh(x / cap) is applied to the natural-domain logit first.
@@ -196,7 +218,7 @@ struct LogitXform {
   float inv_cap;
   float scale_log2;  // scale_nat * log2e (no cap)
   __device__ __forceinline__ float operator()(float dot) const {
-    if (cap > 0.f) return cap * tanhf(dot * scale_nat * inv_cap) * kLog2e;
+    if (cap > 0.f) return cap * tanh_exp(dot * scale_nat * inv_cap) * kLog2e;
     return dot * scale_log2;
   }
 };

@@ -36,38 +36,50 @@
 namespace rpa {
 namespace tc {
 
-constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kThreads = 192;   // warp 0 TMA (+ fp8 decoding), warp 1 MMA, warps 2-5 softmax
 constexpr int kM = 128;         // rows per tile
 constexpr int kN = 128;         // keys per tile
-constexpr int kD = 128;         // head_dim
 constexpr uint32_t kHalf = 128 * 128;          // [128 rows][64 bf16], 16 KB
-constexpr uint32_t kOperand = 2 * kHalf;       // [128 rows][128 bf16] as two halves
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOperand;           // key stage s at kOffK + s*kOperand
-constexpr uint32_t kOffV = 3 * kOperand;       // value stage s at kOffV + s*kOperand
-constexpr uint32_t kOffBar = 5 * kOperand;     // 160 KB
-constexpr int kSmemBytes = (int)kOffBar + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;            // O [0,128), S0 [128,256), S1 [256,384)
 constexpr uint32_t kTmemO = 0, kTmemS = 128;
 constexpr int kRescaleLog2 = 8;
 
+// Shared-memory layout for head_dim D (64 or 128) and cache type.  Operands
+// are [128 rows][D] bf16 in 128-byte swizzled halves of 64 columns.  An fp8
+// cache adds, per stage, staging buffers that receive the pages' e4m3 codes
+// ([128 rows][D] bytes, keys then values) before they are decoded into the
+// bf16 operands.
+template <int D, bool FP8>
+struct TcCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr uint32_t kOperand = kHalves * kHalf;
+  static constexpr uint32_t kStaging = FP8 ? 128u * D : 0u;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOperand;            // key stage s at kOffK + s*kOperand
+  static constexpr uint32_t kOffV = 3 * kOperand;        // value stage s at kOffV + s*kOperand
+  static constexpr uint32_t kOffStg = 5 * kOperand;      // staging (s, kv) at + (2s+kv)*kStaging
+  static constexpr uint32_t kOffBar = (kOffStg + 4 * kStaging + 1023) / 1024 * 1024;
+  static constexpr int kSmemBytes = (int)kOffBar + 256 + 1024;
+};
+
 enum Bar {
   kBarQFull = 0,
-  kBarKFull = 1,    // [2] keys landed
+  kBarKFull = 1,    // [2] key TMA landed
   kBarKEmpty = 3,   // [2] key stage free (S product done)
-  kBarVFull = 5,    // [2] values landed
-  kBarVReady = 7,   // [2] values fixed up, MMA may read
+  kBarVFull = 5,    // [2] value TMA landed
+  kBarVReady = 7,   // [2] values fixed up / decoded, MMA may read
   kBarVEmpty = 9,   // [2] value stage free (PV product done)
   kBarSFull = 11,   // [2] S tile computed
   kBarPReady = 13,  // [2] P written (and O corrected)
   kBarPVDone = 15,  // one arrival per PV product
   kBarODone = 16,   // one arrival per unit, after its last PV product
-  kNumBars = 17,
+  kBarKReady = 17,  // [2] fp8 cache: keys decoded, MMA may read
+  kNumBars = 19,
 };
 
 struct TcMaps {
   CUtensorMap q;      // queries [T][Hq][D], box {64, G, 128/G}
-  CUtensorMap cache;  // pool [num_pages*P][2*Hkv][D], box {64, 1, min(P,128)}
+  CUtensorMap cache;  // pool [num_pages*P][2*Hkv][D], box {64, 1, min(P,128)} (fp8: {D, 1, ..})
   CUtensorMap knew;   // keys [T][Hkv][D], box {64, 1, 128}
   CUtensorMap vnew;   // values [T][Hkv][D], box {64, 1, 128}
 };
@@ -116,8 +128,12 @@ __device__ __forceinline__ UnitGeom unit_geom(const AttnArgs& a, const PrefillUn
   return g;
 }
 
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ TcMaps maps, AttnArgs a) {
+  using C = TcCfg<D, FP8>;
+  constexpr uint32_t kOperand = C::kOperand, kOffQ = C::kOffQ, kOffK = C::kOffK,
+                     kOffV = C::kOffV, kOffBar = C::kOffBar;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -149,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarVEmpty + s), 1);
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarPReady + s), 4);
+      mbar_init(bar(kBarKReady + s), 1);
     }
     mbar_init(bar(kBarPVDone), 1);
     mbar_init(bar(kBarODone), 1);
@@ -170,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem;
 
   const uint32_t idesc_qk = idesc_bf16(kM, kN, false, false);
-  const uint32_t idesc_pv = idesc_bf16(kM, kD, false, true);
+  const uint32_t idesc_pv = idesc_bf16(kM, D, false, true);
   const LogitXform xf{p.softmax_scale * p.k_scale, p.logits_soft_cap,
                       p.logits_soft_cap > 0.f ? 1.f / p.logits_soft_cap : 0.f,
                       p.softmax_scale * p.k_scale * kLog2e};
@@ -193,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // values into value stage j%2 once PV of tile j-2 is done; after the
       // values of a tile land, rows outside its valid range are zeroed.
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kBarQFull), 2 * kHalf);
-        for (int hf = 0; hf < 2; ++hf)
+        mbar_arrive_expect_tx(bar(kBarQFull), kOperand);
+        for (int hf = 0; hf < C::kHalves; ++hf)
           tma_load_3d(sb + kOffQ + hf * kHalf, &maps.q, bar(kBarQFull), hf * 64, g.h * G,
                       g.q0 + g.t_begin);
       }
@@ -211,23 +228,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         return lane < npg ? __ldg(a.kv.block_tables + bt_row + pg0 + lane) : 0;
       };
       // issue the boxes of one operand (kv = 0 keys, 1 values) of tile j; each
-      // lane copies its own page
-      auto issue = [&](int j, int kv, uint32_t dst, uint32_t fullbar, int page) {
+      // lane copies its own page.  New tokens come as bf16 straight into the
+      // operand stage; cached pages too for a bf16 cache, or as e4m3 codes
+      // into the staging buffer for an fp8 cache.
+      auto issue = [&](int j, int kv, uint32_t s, int page) {
         bool is_new;
         int key0, valid;
         g.tile(j, is_new, key0, valid);
+        const uint32_t dst = sb + (kv ? kOffV : kOffK) + s * kOperand;
+        const uint32_t fullbar = bar((kv ? kBarVFull : kBarKFull) + s);
         if (is_new) {
           if (lane == 0) {
-            mbar_arrive_expect_tx(fullbar, 2 * kHalf);
+            mbar_arrive_expect_tx(fullbar, kOperand);
             const int row = g.q0 + (key0 - g.ctx);
-            for (int hf = 0; hf < 2; ++hf)
+            for (int hf = 0; hf < C::kHalves; ++hf)
               tma_load_3d(dst + hf * kHalf, kv ? &maps.vnew : &maps.knew, fullbar, hf * 64, g.h,
                           row);
           }
         } else {
           const int rows = P < kN ? P : kN;
           const int pg0 = key0 / P, npg = (key0 + valid - 1) / P - pg0 + 1;
-          if (lane == 0) mbar_arrive_expect_tx(fullbar, (uint32_t)(npg * rows * 128 * 2));
+          if (lane == 0) mbar_arrive_expect_tx(fullbar, (uint32_t)(npg * rows * D * 2 / (FP8 ? 2 : 1)));
           __syncwarp();
           if (lane < npg) {
             if (page < 0 || page >= p.num_pages) {
@@ -236,31 +257,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int srow = P < kN ? (pg0 + lane) * P - key0 : 0;
             const int z = page * P + (P < kN ? 0 : key0 % P);
-            for (int hf = 0; hf < 2; ++hf)
-              tma_load_3d(dst + hf * kHalf + srow * 128, &maps.cache, fullbar, hf * 64,
-                          2 * g.h + kv, z);
+            if (FP8) {
+              const uint32_t stg = sb + C::kOffStg + (2 * s + kv) * C::kStaging;
+              tma_load_3d(stg + srow * D, &maps.cache, fullbar, 0, 2 * g.h + kv, z);
+            } else {
+              for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_load_3d(dst + hf * kHalf + srow * 128, &maps.cache, fullbar, hf * 64,
+                            2 * g.h + kv, z);
+            }
           }
         }
+      };
+      // fp8 cache: decode a landed operand of tile j into its bf16 stage.
+      // Cached rows are decoded from their e4m3 codes; new rows, which came
+      // as bf16 from the inputs, are quantised and decoded in place so they
+      // carry exactly the codes the page write stores.  Value rows past the
+      // valid range become zero; key rows there are masked by the softmax.
+      auto decode_fp8 = [&](uint32_t s, int j, int kv) {
+        bool is_new;
+        int key0, valid;
+        g.tile(j, is_new, key0, valid);
+        uint8_t* op = smem + (kv ? kOffV : kOffK) + s * kOperand;
+        const uint8_t* stg = smem + C::kOffStg + (2 * s + kv) * C::kStaging;
+        const float scale = kv ? p.v_scale : p.k_scale;
+        const int rows = kv ? kN : valid;
+        for (int idx = lane; idx < rows * (D / 8); idx += 32) {
+          const int r = idx / (D / 8), c = idx % (D / 8);
+          uint4* dst = reinterpret_cast<uint4*>(op + (c >> 3) * kHalf + sw128(r, c & 7));
+          if (r >= valid) {
+            *dst = make_uint4(0, 0, 0, 0);
+          } else if (is_new) {
+            *dst = dequant8(quantize8(*dst, scale));
+          } else {
+            *dst = dequant8(*reinterpret_cast<const uint2*>(stg + r * D + c * 8));
+          }
+        }
+      };
+      auto finalize_k = [&](uint32_t tc, int j) -> bool {
+        const int s = tc & 1;
+        if (!mbar_wait(bar(kBarKFull + s), (tc >> 1) & 1, &s_abort)) return false;
+        decode_fp8(s, j, 0);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarKReady + s));
+        return true;
       };
       auto finalize_v = [&](uint32_t tc, int j) -> bool {
         const int s = tc & 1;
         if (!mbar_wait(bar(kBarVFull + s), (tc >> 1) & 1, &s_abort)) return false;
-        bool is_new;
-        int key0, valid;
-        g.tile(j, is_new, key0, valid);
-        if (valid < kN) {
-          uint8_t* v = smem + kOffV + s * kOperand;
-          for (int idx = lane; idx < (kN - valid) * 16; idx += 32) {
-            const int r = valid + idx / 16, c = idx % 16;  // 16 chunks over both halves
-            *reinterpret_cast<uint4*>(v + (c >> 3) * kHalf + r * 128 + (c & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
+        if (FP8) {
+          decode_fp8(s, j, 1);
           fence_proxy_async();
+        } else {
+          bool is_new;
+          int key0, valid;
+          g.tile(j, is_new, key0, valid);
+          if (valid < kN) {
+            uint8_t* v = smem + kOffV + s * kOperand;
+            for (int idx = lane; idx < (kN - valid) * 8 * C::kHalves; idx += 32) {
+              const int r = valid + idx / (8 * C::kHalves), c = idx % (8 * C::kHalves);
+              *reinterpret_cast<uint4*>(v + (c >> 3) * kHalf + r * 128 + (c & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarVReady + s));
         return true;
       };
+      // Per tile j: keys of j, then (fp8) decode keys of j-1, values of j,
+      // then values of j-1 -- in this order no role waits on another in a
+      // cycle (the MMA needs keys of j+1 before values of j).
       bool ok = true;
       int ids_next = load_ids(0);
       for (int j = 0; j < nt && ok; ++j) {
@@ -273,15 +341,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        issue(j, 0, sb + kOffK + s * kOperand, bar(kBarKFull + s), ids);
+        issue(j, 0, s, ids);
+        if (FP8 && j >= 1) {
+          ok = finalize_k(tc - 1, j - 1);
+          if (!ok) break;
+        }
         if (!mbar_wait(bar(kBarVEmpty + s), par, &s_abort)) {
           ok = false;
           break;
         }
-        issue(j, 1, sb + kOffV + s * kOperand, bar(kBarVFull + s), ids);
+        issue(j, 1, s, ids);
         __syncwarp();
         if (j >= 1) ok = finalize_v(tc - 1, j - 1);
       }
+      if (FP8 && ok && nt >= 1) ok = finalize_k(tcount + nt - 1, nt - 1);
       if (ok && nt >= 1) ok = finalize_v(tcount + nt - 1, nt - 1);
       if (!ok && lane == 0) {
         set_status(hdr, RPA_STATUS_TIMEOUT);
@@ -296,10 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         auto qk = [&](uint32_t tc) -> bool {
           const int s = tc & 1;
-          if (!mbar_wait(bar(kBarKFull + s), (tc >> 1) & 1, &s_abort)) return false;
+          if (!mbar_wait(bar((FP8 ? kBarKReady : kBarKFull) + s), (tc >> 1) & 1, &s_abort))
+            return false;
           tc_fence_after();
           const uint32_t sK = sb + kOffK + s * kOperand;
-          for (int k = 0; k < kD / 16; ++k) {
+          for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
             umma_ss(tmem + kTmemS + 128 * s, sdesc_sw128(sb + kOffQ + off, 16, 1024),
                     sdesc_sw128(sK + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
@@ -350,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // this unit's new tokens -> their pages (one warp per token)
       for (int i = warp - 2; i < g.t_end - g.t_begin; i += 4)
-        write_token_kv<false>(a.kv, g.seq, g.q0 + g.t_begin + i, g.ctx + g.t_begin + i, g.h, lane);
+        write_token_kv<FP8>(a.kv, g.seq, g.q0 + g.t_begin + i, g.ctx + g.t_begin + i, g.h, lane);
 
       float m_run = a.sink ? a.sink[hq] * kLog2e : -INFINITY;
       float l_run = a.sink ? 1.f : 0.f;
@@ -406,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int c0 = 0; c0 < kD; c0 += 32) {
+          for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t oc[32];
             tmem_ld32(tmem + lane_off + kTmemO + c0, oc);
 #pragma unroll
@@ -434,19 +508,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && !mbar_wait(bar(kBarODone), ucount & 1, &s_abort)) ok = false;
       if (ok) {
         tc_fence_after();
-        uint32_t orow[128];
-        tmem_ld128(tmem + lane_off + kTmemO, orow);
-        if (row_valid) {
-          const float inv = p.v_scale / l_run;
-          __nv_bfloat16* dst = a.out + ((int64_t)(g.q0 + g.t_begin + ti) * p.num_q_heads + hq) * kD;
+        const float inv = p.v_scale / l_run;
+        __nv_bfloat16* dst = a.out + ((int64_t)(g.q0 + g.t_begin + ti) * p.num_q_heads + hq) * D;
 #pragma unroll
-          for (int c = 0; c < kD; c += 8) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(orow[c]) * inv, __uint_as_float(orow[c + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(orow[c + 2]) * inv, __uint_as_float(orow[c + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(orow[c + 4]) * inv, __uint_as_float(orow[c + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(orow[c + 6]) * inv, __uint_as_float(orow[c + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c) = v;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t oc[32];
+          tmem_ld32(tmem + lane_off + kTmemO + c0, oc);
+          if (row_valid) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(oc[c]) * inv, __uint_as_float(oc[c + 1]) * inv);
+              v.y = pack_bf16(__uint_as_float(oc[c + 2]) * inv, __uint_as_float(oc[c + 3]) * inv);
+              v.z = pack_bf16(__uint_as_float(oc[c + 4]) * inv, __uint_as_float(oc[c + 5]) * inv);
+              v.w = pack_bf16(__uint_as_float(oc[c + 6]) * inv, __uint_as_float(oc[c + 7]) * inv);
+              *reinterpret_cast<uint4*>(dst + c0 + c) = v;
+            }
           }
         }
       } else if (lane == 0) {
@@ -468,33 +545,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool prefill_uses_tc(const rpa_params_t& p) {
   const int G = p.num_q_heads / p.num_kv_heads;
-  return p.head_dim == 128 && p.kv_dtype == RPA_KV_BF16 && p.page_size >= 8 && G >= 1 && G <= 16;
+  return (p.head_dim == 64 || p.head_dim == 128) && p.page_size >= 8 && G >= 1 && G <= 16;
 }
 
-cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream) {
+template <int D, bool FP8>
+static cudaError_t launch_prefill_tc_t(const AttnArgs& a, int max_units, int num_sms,
+                                       cudaStream_t stream) {
+  using C = tc::TcCfg<D, FP8>;
   static std::atomic<unsigned long long> attr_done{0};
-  auto kern = tc::prefill_tc_kernel;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), tc::kSmemBytes, &attr_done);
+  auto kern = tc::prefill_tc_kernel<D, FP8>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, &attr_done);
   if (e != cudaSuccess) return e;
   const rpa_params_t& p = a.kv.p;
   const int G = p.num_q_heads / p.num_kv_heads;
   tc::TcMaps maps;
   const uint64_t T = (uint64_t)(p.total_tokens > 0 ? p.total_tokens : 1);
   const uint32_t prow = p.page_size < tc::kN ? (uint32_t)p.page_size : (uint32_t)tc::kN;
-  bool ok = encode_map_3d(&maps.q, a.queries, 2, 128, (uint64_t)p.num_q_heads, T, 64u,
-                          (uint32_t)G, (uint32_t)(tc::kM / G), true) &&
-            encode_map_3d(&maps.cache, a.kv.cache, 2, 128, 2 * (uint64_t)p.num_kv_heads,
-                          (uint64_t)p.num_pages * p.page_size, 64u, 1u, prow, true) &&
-            encode_map_3d(&maps.knew, a.kv.keys, 2, 128, (uint64_t)p.num_kv_heads, T, 64u, 1u,
-                          128u, true) &&
-            encode_map_3d(&maps.vnew, a.kv.values, 2, 128, (uint64_t)p.num_kv_heads, T, 64u, 1u,
+  bool ok = encode_map_3d(&maps.q, a.queries, 2, D, (uint64_t)p.num_q_heads, T, 64u, (uint32_t)G,
+                          (uint32_t)(tc::kM / G), true) &&
+            encode_map_3d(&maps.cache, a.kv.cache, FP8 ? 1 : 2, D, 2 * (uint64_t)p.num_kv_heads,
+                          (uint64_t)p.num_pages * p.page_size, FP8 ? (uint32_t)D : 64u, 1u, prow,
+                          !FP8) &&
+            encode_map_3d(&maps.knew, a.kv.keys, 2, D, (uint64_t)p.num_kv_heads, T, 64u, 1u, 128u,
+                          true) &&
+            encode_map_3d(&maps.vnew, a.kv.values, 2, D, (uint64_t)p.num_kv_heads, T, 64u, 1u,
                           128u, true);
   if (!ok) return cudaErrorInvalidValue;
   int grid = num_sms;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
-  kern<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(maps, a);
+  kern<<<grid, tc::kThreads, C::kSmemBytes, stream>>>(maps, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream) {
+  const bool fp8 = a.kv.p.kv_dtype == RPA_KV_FP8_E4M3;
+  if (a.kv.p.head_dim == 64)
+    return fp8 ? launch_prefill_tc_t<64, true>(a, max_units, num_sms, stream)
+               : launch_prefill_tc_t<64, false>(a, max_units, num_sms, stream);
+  return fp8 ? launch_prefill_tc_t<128, true>(a, max_units, num_sms, stream)
+             : launch_prefill_tc_t<128, false>(a, max_units, num_sms, stream);
 }
 
 }  // namespace rpa

@@ -400,6 +400,28 @@ def fp8() -> Workload:
                     total_tokens=int(q.sum()))
 
 
+def fp8_small() -> Workload:
+    """The fp8 workload's shape and options with 64 decode sequences (profiling size)."""
+    seed = 1015
+    g = torch.Generator().manual_seed(seed)
+    P = 16
+    dec_kv = _randint(g, 256, 16384, 64)
+    chunk_ctx = _randint(g, 0, 8192, 8)
+    q = np.concatenate([np.ones(64, np.int32), np.full(8, 256, np.int32)])
+    kv = np.concatenate([dec_kv, chunk_ctx + 256]).astype(np.int32)
+    need = int(sum(-(-int(k) // P) for k in kv))
+    num_pages = int(math.ceil(need * 1.1))
+    pps = -(-max(16384, 8192 + 256) // P)
+    bt = _assign_pages(kv, P, num_pages, len(q), pps, g)
+    return Workload(name="fp8_small", seed=seed, num_q_heads=64, num_kv_heads=8, head_dim=64,
+                    page_size=P, num_pages=num_pages, pages_per_seq=pps, max_num_seqs=len(q),
+                    kv_dtype="fp8", softmax_scale=1.0 / 8.0, sliding_window=128,
+                    logits_soft_cap=30.0, k_scale=0.05, v_scale=0.05, has_sink=True,
+                    q_lens=q, kv_lens_valid=kv, block_tables=bt,
+                    distribution=np.array([64, 72, 72], np.int32),
+                    total_tokens=int(q.sum()))
+
+
 WORKLOADS = {
     "tiny": tiny,
     "decode": decode,
@@ -409,6 +431,7 @@ WORKLOADS = {
     "long_w4096": lambda: long(4096),
     "long_small": long_small,
     "fp8": fp8,
+    "fp8_small": fp8_small,
 }
 
 
