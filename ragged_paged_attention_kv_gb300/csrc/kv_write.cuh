@@ -59,6 +59,52 @@ __device__ __forceinline__ void write_token_kv(const KvArgs& a, int seq, int t, 
   }
 }
 
+// One warp writes key and value head `h` of the n consecutive input tokens
+// t0 .. t0+n-1 (positions pos0 .. pos0+n-1 of sequence `seq`) into the pool.
+// Lanes take consecutive 16-byte chunks (a token's key row, then its value
+// row), and each lane issues the block-table and input loads of kBatch
+// chunks before any of their stores, so the loads' latencies overlap.
+template <bool FP8, int D, int kBatch>
+__device__ __forceinline__ void write_tokens_kv(const KvArgs& a, int seq, int t0, int pos0, int n,
+                                                int h, int lane) {
+  constexpr int kChunks = D / 8;       // 16-byte chunks of one bf16 row
+  constexpr int kItems = 2 * kChunks;  // key and value chunks of one token
+  const int total = n * kItems;
+  const int32_t* bt = a.block_tables + (int64_t)seq * a.p.pages_per_seq;
+  for (int base = 0; base < total; base += 32 * kBatch) {
+    uint4 x[kBatch];
+    int32_t page[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + 32 * b + lane;
+      if (idx < total) {
+        const int i = idx / kItems, kv = (idx % kItems) / kChunks, c = idx % kChunks;
+        page[b] = __ldg(bt + (pos0 + i) / a.p.page_size);
+        x[b] = __ldg(reinterpret_cast<const uint4*>(
+            (kv ? a.values : a.keys) + ((int64_t)(t0 + i) * a.p.num_kv_heads + h) * D + c * 8));
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int idx = base + 32 * b + lane;
+      if (idx >= total) continue;
+      if (page[b] < 0 || page[b] >= a.p.num_pages) {
+        set_status(a.ws, RPA_STATUS_BAD_PAGE);
+        continue;
+      }
+      const int i = idx / kItems, kv = (idx % kItems) / kChunks, c = idx % kChunks;
+      const int pos = pos0 + i;
+      const int64_t dst = pool_offset(a.p, page[b], pos % a.p.page_size, 2 * h + kv, FP8 ? 1 : 2);
+      if (FP8) {
+        *reinterpret_cast<uint2*>(a.cache + dst + c * 8) =
+            quantize8(x[b], kv ? a.p.v_scale : a.p.k_scale);
+      } else {
+        *reinterpret_cast<uint4*>(a.cache + dst + c * 16) = x[b];
+      }
+    }
+  }
+}
+
 // Arguments of the attention kernels.
 struct AttnArgs {
   KvArgs kv;

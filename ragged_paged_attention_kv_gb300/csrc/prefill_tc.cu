@@ -422,9 +422,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = g.ctx + i_tok;
       const int hq = g.h * G + r % G;
 
-      // this unit's new tokens -> their pages (one warp per token)
-      for (int i = warp - 2; i < g.t_end - g.t_begin; i += 4)
-        write_token_kv<FP8>(a.kv, g.seq, g.q0 + g.t_begin + i, g.ctx + g.t_begin + i, g.h, lane);
+      // this unit's new tokens -> their pages (a quarter of them per warp);
+      // the loads are batched, so the write fits in the time the first S
+      // tile of the unit takes to arrive
+      {
+        const int n = g.t_end - g.t_begin, w = warp - 2;
+        const int i0 = n * w / 4, i1 = n * (w + 1) / 4;
+        write_tokens_kv<FP8, D, 4>(a.kv, g.seq, g.q0 + g.t_begin + i0, g.ctx + g.t_begin + i0,
+                                   i1 - i0, g.h, lane);
+      }
 
       float m_run = a.sink ? a.sink[hq] * kLog2e : -INFINITY;
       float l_run = a.sink ? 1.f : 0.f;
