@@ -465,7 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < kN; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(sr[c]));
+        for (int c = 0; c < kN; c += 2)
+          mx[(c >> 1) & 3] =
+              max3f(mx[(c >> 1) & 3], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
         const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
         // lazy rescale: move the max only when it grows by more than 2^8
         const bool need = mt > m_run + (float)kRescaleLog2;
@@ -495,16 +497,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float nm = m_run == -INFINITY ? 0.f : -m_run;
-        float rs[4] = {0.f, 0.f, 0.f, 0.f};
-        // P packed as bf16 pairs into sr[0..64): sr[c/2] is already consumed
+        const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(nm, nm);
+        uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+        // P packed as bf16 pairs into sr[0..64): sr[c/2] is already consumed.
+        // Scale-and-subtract and the row sums use packed f32x2 arithmetic
+        // (one instruction per pair), the exponentials the hardware ex2.
 #pragma unroll
         for (int c = 0; c < kN; c += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c]), sc, nm));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c + 1]), sc, nm));
-          rs[(c >> 1) & 3] += p0 + p1;
+          const uint64_t x2 =
+              f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nm2);
+          float x0, x1;
+          f2_unpack(x2, x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          rs2[(c >> 1) & 1] = f2_add(rs2[(c >> 1) & 1], f2_pack(p0, p1));
           sr[c >> 1] = pack_bf16(p0, p1);
         }
-        l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(rs2[0], a0, a1);
+          f2_unpack(rs2[1], b0, b1);
+          l_run += (a0 + a1) + (b0 + b1);
+        }
         tmem_st64p(tmem + lane_off + kTmemS + 128 * s, sr);
         tc_fence_before();
         __syncwarp();
