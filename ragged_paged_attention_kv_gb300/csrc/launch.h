@@ -20,7 +20,7 @@ bool prefill_uses_tc(const rpa_params_t& p);
 cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
 
 // Rows of a prefill tile for these params (the planner and the kernels agree on it).
-inline int prefill_rows_for(const rpa_params_t& p) { return prefill_uses_tc(p) ? 128 : kPrefillRows; }
+inline int prefill_rows_for(const rpa_params_t& p) { return prefill_uses_tc(p) ? 256 : kPrefillRows; }
 
 // plan -> decode -> prefill on `stream`; events (4, or null) are recorded
 // before the planner and after each kernel.

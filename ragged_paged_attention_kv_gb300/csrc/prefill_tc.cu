@@ -1,25 +1,28 @@
 // Prefill / chunked-prefill path on the 5th-generation tensor cores.
 //
-// Work unit = (sequence, tile of new tokens, kv head).  The tile's 128 rows
-// are (token, q-head of the GQA group) pairs, token-major (row r is token
-// t_begin + r / G, q-head h*G + r % G), as tpu-inference RPA v3 kernel.py
-// stacks a q block's heads of one kv head, so every key/value tile serves all
-// G heads.  Per 128-key tile:
-//   S = Q K^T      tcgen05.mma, A = Q and B = K from 128-byte swizzled shared
-//                  memory, fp32 accumulator in tensor memory (two S buffers,
-//                  so the next tile's S overlaps this tile's softmax);
-//   P = softmax    one thread per row reads S from tensor memory, applies
-//                  scale / soft cap / causal + window mask, keeps the running
-//                  max m and sum l in fp32 (RPA v3
+// Work unit = (sequence, run of new tokens, kv head) of 256 rows: two tiles
+// A and B of 128 (token, q-head of the GQA group) rows each, token-major (row
+// R is token t_begin + R / G, q-head h*G + R % G), as tpu-inference RPA v3
+// kernel.py stacks a q block's heads of one kv head, so every key/value tile
+// serves all G heads of both tiles.  Per 128-key tile j and each of A, B:
+//   S = Q K^T      tcgen05.mma, A operand = the tile's queries and B operand
+//                  = the keys, from 128-byte swizzled shared memory; fp32
+//                  accumulator in tensor memory;
+//   P = softmax    one thread per row (a warpgroup per tile) reads S from
+//                  tensor memory, applies scale / soft cap / causal + window
+//                  mask, keeps the running max m and sum l in fp32 (RPA v3
 //                  flash_attention_step1_qk_softmax), and writes P as bf16
 //                  back over S;
-//   O += P V       tcgen05.mma with A = P from tensor memory and B = V from
-//                  shared memory (RPA v3 flash_attention_step2_pv); O stays
-//                  in tensor memory and is rescaled there only when a row's
-//                  max grows by more than 2^8.
-// The RPA v3 kernel overlaps step2 of one kv head with step1 of the next;
-// here a producer warp (TMA), an MMA warp and a softmax warpgroup run
-// concurrently, synchronised by mbarriers, which overlaps the same stages.
+//   O += P V       tcgen05.mma with A operand = P from tensor memory and B =
+//                  the values (RPA v3 flash_attention_step2_pv); O stays in
+//                  tensor memory and is rescaled there only when a row's max
+//                  grows by more than 2^8.
+// The RPA v3 kernel overlaps step2 of one kv head with step1 of the next.
+// Here the two tiles play that part: the MMA thread issues PV_A(j), S_A(j+1),
+// PV_B(j), S_B(j+1), so the tensor core works on one tile while the other
+// tile's warpgroup computes its softmax (the ping-pong FlashAttention-4 uses
+// on Blackwell).  A TMA warp feeds two-stage key and value rings; the keys
+// and values of a tile are fetched once for both query tiles.
 //
 // Keys come in two kinds of tiles: cached keys [lo, ctx) are fetched page by
 // page from the pool (one TMA box per page and 64-wide half of head_dim);
@@ -36,44 +39,55 @@
 namespace rpa {
 namespace tc {
 
-constexpr int kThreads = 192;   // warp 0 TMA (+ fp8 decoding), warp 1 MMA, warps 2-5 softmax
-constexpr int kM = 128;         // rows per tile
+// warpgroup 0: warp 0 TMA (+ fp8 decoding), warp 1 MMA, warps 2-3 idle;
+// warpgroups 1 and 2: softmax of query tiles A and B
+constexpr int kThreads = 384;
+constexpr int kM = 128;         // rows per query tile (two per unit)
 constexpr int kN = 128;         // keys per tile
 constexpr uint32_t kHalf = 128 * 128;          // [128 rows][64 bf16], 16 KB
-constexpr uint32_t kTmemCols = 512;            // O [0,128), S0 [128,256), S1 [256,384)
-constexpr uint32_t kTmemO = 0, kTmemS = 128;
+constexpr uint32_t kTmemCols = 512;            // O_A, O_B, S_A, S_B: 128 columns each
+constexpr uint32_t kTmemO = 0, kTmemS = 256;   // tile X: O at kTmemO + 128X, S at kTmemS + 128X
 constexpr int kRescaleLog2 = 8;
+// registers per thread after the split: the launch gives 384 x 168; the
+// TMA/MMA warpgroup drops to 40 and the softmax warpgroups take the rest
+constexpr int kRegsControl = 40, kRegsSoftmax = 232;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
 
 // Shared-memory layout for head_dim D (64 or 128) and cache type.  Operands
-// are [128 rows][D] bf16 in 128-byte swizzled halves of 64 columns.  An fp8
-// cache adds, per stage, staging buffers that receive the pages' e4m3 codes
-// ([128 rows][D] bytes, keys then values) before they are decoded into the
-// bf16 operands.
+// are [128 rows][D] bf16 in 128-byte swizzled halves of 64 columns: query
+// tiles A and B, then two key and two value stages.  An fp8 cache adds
+// staging buffers that receive the pages' e4m3 codes ([128 rows][D] bytes)
+// before they are decoded into the bf16 operands: one per stage and operand
+// where they fit, else one per operand (head_dim 128).
 template <int D, bool FP8>
 struct TcCfg {
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kOperand = kHalves * kHalf;
   static constexpr uint32_t kStaging = FP8 ? 128u * D : 0u;
-  static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOperand;            // key stage s at kOffK + s*kOperand
-  static constexpr uint32_t kOffV = 3 * kOperand;        // value stage s at kOffV + s*kOperand
-  static constexpr uint32_t kOffStg = 5 * kOperand;      // staging (s, kv) at + (2s+kv)*kStaging
-  static constexpr uint32_t kOffBar = (kOffStg + 4 * kStaging + 1023) / 1024 * 1024;
+  static constexpr uint32_t bytes_for(int stg) {
+    return (6 * kOperand + 2 * stg * kStaging + 1023) / 1024 * 1024 + 256 + 1024;
+  }
+  static constexpr int kStgPerOp = !FP8 ? 0 : (bytes_for(2) <= 227 * 1024 ? 2 : 1);
+  static constexpr uint32_t kOffQ = 0;                  // query tile X at kOffQ + X*kOperand
+  static constexpr uint32_t kOffK = 2 * kOperand;       // key stage s at kOffK + s*kOperand
+  static constexpr uint32_t kOffV = 4 * kOperand;       // value stage s at kOffV + s*kOperand
+  static constexpr uint32_t kOffStg = 6 * kOperand;     // staging (b, kv) at + (2b+kv)*kStaging
+  static constexpr uint32_t kOffBar = (kOffStg + 2 * kStgPerOp * kStaging + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = (int)kOffBar + 256 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "fits one CTA's shared memory");
 };
 
 enum Bar {
-  kBarQFull = 0,
+  kBarQFull = 0,    // both query tiles landed
   kBarKFull = 1,    // [2] key TMA landed
-  kBarKEmpty = 3,   // [2] key stage free (S product done)
+  kBarKEmpty = 3,   // [2] key stage free (S products of both tiles done)
   kBarVFull = 5,    // [2] value TMA landed
   kBarVReady = 7,   // [2] values fixed up / decoded, MMA may read
-  kBarVEmpty = 9,   // [2] value stage free (PV product done)
-  kBarSFull = 11,   // [2] S tile computed
-  kBarPReady = 13,  // [2] P written (and O corrected)
-  kBarPVDone = 15,  // one arrival per PV product
-  kBarODone = 16,   // one arrival per unit, after its last PV product
-  kBarKReady = 17,  // [2] fp8 cache: keys decoded, MMA may read
+  kBarVEmpty = 9,   // [2] value stage free (PV products of both tiles done)
+  kBarKReady = 11,  // [2] fp8 cache: keys decoded, MMA may read
+  kBarSFull = 13,   // [2] per query tile: S computed
+  kBarPReady = 15,  // [2] per query tile: P written (and O corrected)
+  kBarODone = 17,   // [2] per query tile: the unit's last PV product done
   kNumBars = 19,
 };
 
@@ -163,12 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarVFull + s), 1);
       mbar_init(bar(kBarVReady + s), 1);
       mbar_init(bar(kBarVEmpty + s), 1);
+      mbar_init(bar(kBarKReady + s), 1);
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarPReady + s), 4);
-      mbar_init(bar(kBarKReady + s), 1);
+      mbar_init(bar(kBarODone + s), 1);
     }
-    mbar_init(bar(kBarPVDone), 1);
-    mbar_init(bar(kBarODone), 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -194,26 +207,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool has_cap = p.logits_soft_cap > 0.f;
   const float sc = has_cap ? 1.f : xf.scale_log2;  // raw score -> log2-domain logit
 
-  uint32_t tcount = 0;  // tiles processed by this CTA so far (all roles agree)
-  uint32_t ucount = 0;  // units processed by this CTA so far
-  for (;;) {
-    if (tid == 0) s_unit = atomicAdd(hdr + kHdrPrefillNext, 1);
-    __syncthreads();
-    const int u = s_unit;
-    if (u >= n_units || s_abort) break;
-    const UnitGeom g = unit_geom(a, units[u]);
-    const int nt = g.n_tiles;
+  // Every role runs this loop over the CTA's units with its own body, so
+  // the code of each role stays within its register budget; all threads meet
+  // at the same two barriers per unit.  tcount counts the key tiles and
+  // ucount the units the CTA has processed so far (all roles agree).
+  auto unit_loop = [&](auto&& body) {
+    uint32_t tcount = 0, ucount = 0;
+    for (;;) {
+      if (tid == 0) s_unit = atomicAdd(hdr + kHdrPrefillNext, 1);
+      __syncthreads();
+      const int u = s_unit;
+      if (u >= n_units || s_abort) break;
+      const UnitGeom g = unit_geom(a, units[u]);
+      body(g, tcount, ucount);
+      tcount += g.n_tiles;
+      ucount += 1;
+      tc_fence_before();
+      __syncthreads();  // the next unit reuses Q, the stages and tensor memory
+      tc_fence_after();
+    }
+  };
 
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (warp == 0) {
+      unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t ucount) {
+      const int nt = g.n_tiles;
       // ------------------------------------------------------- TMA producer
-      // Keys of tile j go into key stage j%2 once S of tile j-2 is done;
-      // values into value stage j%2 once PV of tile j-2 is done; after the
-      // values of a tile land, rows outside its valid range are zeroed.
+      // Keys of tile j go into key stage j%2 once both S products of tile
+      // j-2 are done; values into value stage j%2 once both PV products of
+      // tile j-2 are done; after the values of a tile land, rows outside its
+      // valid range are zeroed.
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kBarQFull), kOperand);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(sb + kOffQ + hf * kHalf, &maps.q, bar(kBarQFull), hf * 64, g.h * G,
-                      g.q0 + g.t_begin);
+        mbar_arrive_expect_tx(bar(kBarQFull), 2 * kOperand);
+        for (int x = 0; x < 2; ++x)
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(sb + kOffQ + x * kOperand + hf * kHalf, &maps.q, bar(kBarQFull),
+                        hf * 64, g.h * G, g.q0 + g.t_begin + x * (kM / G));
       }
       // Page ids of a cached tile: lane l holds page pg0 + l (a tile spans at
       // most 128/P + 1 <= 17 pages for P >= 8), loaded one tile ahead so the
@@ -227,11 +257,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pg0 = key0 / P, npg = (key0 + valid - 1) / P - pg0 + 1;
         return lane < npg ? __ldg(a.kv.block_tables + bt_row + pg0 + lane) : 0;
       };
+      // staging buffer of an fp8 operand of tile tc
+      auto staging = [&](uint32_t tc, int kv) -> uint32_t {
+        return C::kOffStg + (2 * (C::kStgPerOp == 2 ? (tc & 1) : 0) + kv) * C::kStaging;
+      };
       // issue the boxes of one operand (kv = 0 keys, 1 values) of tile j; each
       // lane copies its own page.  New tokens come as bf16 straight into the
       // operand stage; cached pages too for a bf16 cache, or as e4m3 codes
       // into the staging buffer for an fp8 cache.
-      auto issue = [&](int j, int kv, uint32_t s, int page) {
+      auto issue = [&](int j, int kv, uint32_t tc, int page) {
+        const uint32_t s = tc & 1;
         bool is_new;
         int key0, valid;
         g.tile(j, is_new, key0, valid);
@@ -258,8 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int srow = P < kN ? (pg0 + lane) * P - key0 : 0;
             const int z = page * P + (P < kN ? 0 : key0 % P);
             if (FP8) {
-              const uint32_t stg = sb + C::kOffStg + (2 * s + kv) * C::kStaging;
-              tma_load_3d(stg + srow * D, &maps.cache, fullbar, 0, 2 * g.h + kv, z);
+              tma_load_3d(sb + staging(tc, kv) + srow * D, &maps.cache, fullbar, 0, 2 * g.h + kv, z);
             } else {
               for (int hf = 0; hf < C::kHalves; ++hf)
                 tma_load_3d(dst + hf * kHalf + srow * 128, &maps.cache, fullbar, hf * 64,
@@ -273,12 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // as bf16 from the inputs, are quantised and decoded in place so they
       // carry exactly the codes the page write stores.  Value rows past the
       // valid range become zero; key rows there are masked by the softmax.
-      auto decode_fp8 = [&](uint32_t s, int j, int kv) {
+      auto decode_fp8 = [&](uint32_t tc, int j, int kv) {
         bool is_new;
         int key0, valid;
         g.tile(j, is_new, key0, valid);
-        uint8_t* op = smem + (kv ? kOffV : kOffK) + s * kOperand;
-        const uint8_t* stg = smem + C::kOffStg + (2 * s + kv) * C::kStaging;
+        uint8_t* op = smem + (kv ? kOffV : kOffK) + (tc & 1) * kOperand;
+        const uint8_t* stg = smem + staging(tc, kv);
         const float scale = kv ? p.v_scale : p.k_scale;
         const int rows = kv ? kN : valid;
         for (int idx = lane; idx < rows * (D / 8); idx += 32) {
@@ -296,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto finalize_k = [&](uint32_t tc, int j) -> bool {
         const int s = tc & 1;
         if (!mbar_wait(bar(kBarKFull + s), (tc >> 1) & 1, &s_abort)) return false;
-        decode_fp8(s, j, 0);
+        decode_fp8(tc, j, 0);
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarKReady + s));
@@ -306,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = tc & 1;
         if (!mbar_wait(bar(kBarVFull + s), (tc >> 1) & 1, &s_abort)) return false;
         if (FP8) {
-          decode_fp8(s, j, 1);
+          decode_fp8(tc, j, 1);
           fence_proxy_async();
         } else {
           bool is_new;
@@ -328,7 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // Per tile j: keys of j, then (fp8) decode keys of j-1, values of j,
       // then values of j-1 -- in this order no role waits on another in a
-      // cycle (the MMA needs keys of j+1 before values of j).
+      // cycle (the MMA needs keys of j+1 before the values of j are used by
+      // the second query tile).  With one staging buffer per operand the
+      // codes of tile j-1 are decoded before those of tile j are fetched.
+      constexpr bool kStg1 = FP8 && C::kStgPerOp == 1;
       bool ok = true;
       int ids_next = load_ids(0);
       for (int j = 0; j < nt && ok; ++j) {
@@ -337,22 +374,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t par = ((tc >> 1) & 1) ^ 1;
         const int ids = ids_next;
         if (j + 1 < nt) ids_next = load_ids(j + 1);
+        if (kStg1 && j >= 1) {
+          ok = finalize_k(tc - 1, j - 1);
+          if (!ok) break;
+        }
         if (!mbar_wait(bar(kBarKEmpty + s), par, &s_abort)) {
           ok = false;
           break;
         }
-        issue(j, 0, s, ids);
-        if (FP8 && j >= 1) {
+        issue(j, 0, tc, ids);
+        if (FP8 && !kStg1 && j >= 1) {
           ok = finalize_k(tc - 1, j - 1);
+          if (!ok) break;
+        }
+        if (kStg1 && j >= 1) {
+          ok = finalize_v(tc - 1, j - 1);
           if (!ok) break;
         }
         if (!mbar_wait(bar(kBarVEmpty + s), par, &s_abort)) {
           ok = false;
           break;
         }
-        issue(j, 1, s, ids);
+        issue(j, 1, tc, ids);
         __syncwarp();
-        if (j >= 1) ok = finalize_v(tc - 1, j - 1);
+        if (!kStg1 && j >= 1) ok = finalize_v(tc - 1, j - 1);
       }
       if (FP8 && ok && nt >= 1) ok = finalize_k(tcount + nt - 1, nt - 1);
       if (ok && nt >= 1) ok = finalize_v(tcount + nt - 1, nt - 1);
@@ -360,74 +405,100 @@ __global__ void __launch_bounds__(kThreads, 1)
         set_status(hdr, RPA_STATUS_TIMEOUT);
         s_abort = 1;
       }
+      });
     } else if (warp == 1) {
+      unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t ucount) {
+      const int nt = g.n_tiles;
+      const bool has_b = g.t_begin + kM / G < g.t_end;
       // ------------------------------------------------------------ MMA
-      // Order: S(0), then for each tile j: S(j+1), PV(j) -- the next tile's
-      // scores are computed while the softmax warps work on tile j.
+      // Order: S_A(0), S_B(0), then for each tile j: PV_A(j), S_A(j+1),
+      // PV_B(j), S_B(j+1).  S_X(j+1) overwrites P_X(j) only after PV_X(j)
+      // has read it (the tensor core runs one thread's products in order),
+      // and its completion also tells the softmax of tile X that PV_X(j) is
+      // done, so O_X may be rescaled.
       if (lane == 0) {
         bool ok = mbar_wait(bar(kBarQFull), ucount & 1, &s_abort);
         tc_fence_after();
-        auto qk = [&](uint32_t tc) -> bool {
+        auto qk = [&](uint32_t tc, int x, bool last_of_stage) -> bool {
           const int s = tc & 1;
-          if (!mbar_wait(bar((FP8 ? kBarKReady : kBarKFull) + s), (tc >> 1) & 1, &s_abort))
-            return false;
-          tc_fence_after();
+          if (x == 0) {
+            if (!mbar_wait(bar((FP8 ? kBarKReady : kBarKFull) + s), (tc >> 1) & 1, &s_abort))
+              return false;
+            tc_fence_after();
+          }
           const uint32_t sK = sb + kOffK + s * kOperand;
+          const uint32_t sQ = sb + kOffQ + x * kOperand;
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-            umma_ss(tmem + kTmemS + 128 * s, sdesc_sw128(sb + kOffQ + off, 16, 1024),
+            umma_ss(tmem + kTmemS + 128 * x, sdesc_sw128(sQ + off, 16, 1024),
                     sdesc_sw128(sK + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
           }
-          umma_commit(bar(kBarKEmpty + s));
-          umma_commit(bar(kBarSFull + s));
+          umma_commit(bar(kBarSFull + x));
+          if (last_of_stage) umma_commit(bar(kBarKEmpty + s));
           return true;
         };
-        auto pv = [&](uint32_t tc, int j) -> bool {
+        auto pv = [&](uint32_t tc, int j, int x, bool last_of_stage) -> bool {
           const int s = tc & 1;
-          if (!mbar_wait(bar(kBarPReady + s), (tc >> 1) & 1, &s_abort)) return false;
-          if (!mbar_wait(bar(kBarVReady + s), (tc >> 1) & 1, &s_abort)) return false;
+          if (!mbar_wait(bar(kBarPReady + x), tc & 1, &s_abort)) return false;
+          if (x == 0 && !mbar_wait(bar(kBarVReady + s), (tc >> 1) & 1, &s_abort)) return false;
           tc_fence_after();
           const uint32_t sV = sb + kOffV + s * kOperand;
           for (int k = 0; k < kN / 16; ++k) {
             const uint64_t bd = sdesc_sw128(sV + k * 16 * 128, kHalf, 1024);
-            umma_ts(tmem + kTmemO, tmem + kTmemS + 128 * s + 8 * k, bd, idesc_pv,
+            umma_ts(tmem + kTmemO + 128 * x, tmem + kTmemS + 128 * x + 8 * k, bd, idesc_pv,
                     (j > 0 || k > 0) ? 1u : 0u);
           }
-          umma_commit(bar(kBarVEmpty + s));
-          umma_commit(bar(kBarPVDone));
+          if (last_of_stage) umma_commit(bar(kBarVEmpty + s));
           return true;
         };
-        if (ok && nt >= 1) ok = qk(tcount);
+        if (ok && nt >= 1) ok = qk(tcount, 0, !has_b);
+        if (ok && nt >= 1 && has_b) ok = qk(tcount, 1, true);
         for (int j = 0; j < nt && ok; ++j) {
-          if (j + 1 < nt) ok = qk(tcount + j + 1);
-          if (ok) ok = pv(tcount + j, j);
+          const uint32_t tc = tcount + j;
+          ok = pv(tc, j, 0, !has_b);
+          if (ok && j + 1 == nt) umma_commit(bar(kBarODone + 0));
+          if (ok && j + 1 < nt) ok = qk(tc + 1, 0, !has_b);
+          if (ok && has_b) {
+            ok = pv(tc, j, 1, true);
+            if (ok && j + 1 == nt) umma_commit(bar(kBarODone + 1));
+            if (ok && j + 1 < nt) ok = qk(tc + 1, 1, true);
+          }
         }
-        // A parity wait only tells the current phase from the previous one,
-        // so the epilogue, which may be two PV products ahead of PVDone,
-        // waits on this once-per-unit barrier instead.
-        if (ok) umma_commit(bar(kBarODone));
         if (!ok) {
           set_status(hdr, RPA_STATUS_TIMEOUT);
           s_abort = 1;
         }
       }
+      });
     } else {
-      // --------------------------------------------------- softmax warps
+      unit_loop([](const UnitGeom&, uint32_t, uint32_t) {});
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t ucount) {
+    const int nt = g.n_tiles;
+    // tile B holds tokens t_begin + 128/G onwards; it may be empty
+    const bool has_b = g.t_begin + kM / G < g.t_end;
+    if (warp < 8 || has_b) {
+      // ---------------------------------------------- softmax of tile x
+      const int x = (warp - 4) >> 2;           // query tile of this warpgroup
       const int q4 = warp & 3;                 // tensor-memory lane quarter
       const int r = 32 * q4 + lane;            // row of the tile
       const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-      const int ti = r / G;
+      const int ti = (kM * x + r) / G;         // token of the row, from t_begin
       const bool row_valid = g.t_begin + ti < g.t_end;
       const int i_tok = g.t_begin + min(ti, g.t_end - g.t_begin - 1);
       const int pos = g.ctx + i_tok;
       const int hq = g.h * G + r % G;
+      const uint32_t tS = tmem + lane_off + kTmemS + 128 * x;
+      const uint32_t tO = tmem + lane_off + kTmemO + 128 * x;
 
-      // this unit's new tokens -> their pages (a quarter of them per warp);
-      // the loads are batched, so the write fits in the time the first S
-      // tile of the unit takes to arrive
+      // this unit's new tokens -> their pages (an eighth of them per warp, a
+      // quarter when tile B is empty); the loads are batched, so the write
+      // fits in the time the first S tile of the unit takes to arrive
       {
-        const int n = g.t_end - g.t_begin, w = warp - 2;
-        const int i0 = n * w / 4, i1 = n * (w + 1) / 4;
+        const int n = g.t_end - g.t_begin, nw = has_b ? 8 : 4, w = warp - 4;
+        const int i0 = n * w / nw, i1 = n * (w + 1) / nw;
         write_tokens_kv<FP8, D, 4>(a.kv, g.seq, g.q0 + g.t_begin + i0, g.ctx + g.t_begin + i0,
                                    i1 - i0, g.h, lane);
       }
@@ -437,8 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
         const uint32_t tc = tcount + j;
-        const int s = tc & 1;
-        if (!mbar_wait(bar(kBarSFull + s), (tc >> 1) & 1, &s_abort)) {
+        if (!mbar_wait(bar(kBarSFull + x), tc & 1, &s_abort)) {
           ok = false;
           break;
         }
@@ -447,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int key0, valid;
         g.tile(j, is_new, key0, valid);
         uint32_t sr[128];
-        tmem_ld128(tmem + lane_off + kTmemS + 128 * s, sr);
+        tmem_ld128(tS, sr);
         const bool full = valid == kN && key0 + kN - 1 <= pos && (W == 0 || pos - key0 < W);
         // logits in the log2 domain are fma(s, sc, -m): with a soft cap the
         // capped logit is formed first and sc is 1
@@ -478,22 +548,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= alpha;
         }
         if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // O must hold P V of every earlier tile before it is rescaled.  The
-          // parity wait is exact here: S of this tile was committed after PV of
-          // tile tc-2, and PV of this tile needs our P, so PVDone has completed
-          // either tc-1 or tc phases.
-          if (!mbar_wait(bar(kBarPVDone), (tc - 1) & 1, &s_abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          // O holds P V of every earlier tile: S_X(j) completed after PV_X(j-1)
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t oc[32];
-            tmem_ld32(tmem + lane_off + kTmemO + c0, oc);
+            tmem_ld32(tO + c0, oc);
 #pragma unroll
             for (int c = 0; c < 32; ++c) oc[c] = __float_as_uint(__uint_as_float(oc[c]) * alpha);
-            tmem_st32p(tmem + lane_off + kTmemO + c0, oc);
+            tmem_st32p(tO + c0, oc);
           }
         }
         const float nm = m_run == -INFINITY ? 0.f : -m_run;
@@ -518,13 +580,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_unpack(rs2[1], b0, b1);
           l_run += (a0 + a1) + (b0 + b1);
         }
-        tmem_st64p(tmem + lane_off + kTmemS + 128 * s, sr);
+        tmem_st64p(tS, sr);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPReady + s));
+        if (lane == 0) mbar_arrive(bar(kBarPReady + x));
       }
       // epilogue: O / l -> bf16 rows
-      if (ok && !mbar_wait(bar(kBarODone), ucount & 1, &s_abort)) ok = false;
+      if (ok && !mbar_wait(bar(kBarODone + x), ucount & 1, &s_abort)) ok = false;
       if (ok) {
         tc_fence_after();
         const float inv = p.v_scale / l_run;
@@ -532,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t oc[32];
-          tmem_ld32(tmem + lane_off + kTmemO + c0, oc);
+          tmem_ld32(tO + c0, oc);
           if (row_valid) {
 #pragma unroll
             for (int c = 0; c < 32; c += 8) {
@@ -550,11 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_abort = 1;
       }
     }
-    tcount += nt;
-    ucount += 1;
-    tc_fence_before();
-    __syncthreads();  // the next unit reuses Q, the stages and tensor memory
-    tc_fence_after();
+    });
   }
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
