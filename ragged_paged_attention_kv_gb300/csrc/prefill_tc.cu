@@ -49,8 +49,9 @@ constexpr uint32_t kTmemCols = 512;            // O_A, O_B, S_A, S_B: 128 column
 constexpr uint32_t kTmemO = 0, kTmemS = 256;   // tile X: O at kTmemO + 128X, S at kTmemS + 128X
 constexpr int kRescaleLog2 = 8;
 // registers per thread after the split: the launch gives 384 x 168; the
-// TMA/MMA warpgroup drops to 40 and the softmax warpgroups take the rest
-constexpr int kRegsControl = 40, kRegsSoftmax = 232;
+// TMA/MMA warpgroup drops to 56 and the softmax warpgroups take 224 (no
+// role spills at this split)
+constexpr int kRegsControl = 56, kRegsSoftmax = 224;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
 
 // Shared-memory layout for head_dim D (64 or 128) and cache type.  Operands
@@ -549,13 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // O holds P V of every earlier tile: S_X(j) completed after PV_X(j-1)
+          // in chunks of 16 columns: the S tile is live in registers meanwhile
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t oc[32];
-            tmem_ld32(tO + c0, oc);
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t oc[16];
+            tmem_ld16(tO + c0, oc);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) oc[c] = __float_as_uint(__uint_as_float(oc[c]) * alpha);
-            tmem_st32p(tO + c0, oc);
+            for (int c = 0; c < 16; ++c) oc[c] = __float_as_uint(__uint_as_float(oc[c]) * alpha);
+            tmem_st16(tO + c0, oc);
           }
         }
         const float nm = m_run == -INFINITY ? 0.f : -m_run;
