@@ -330,7 +330,13 @@ def gpu_arm(args, world, rank, local):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     else:
-        kernel, kfile = "prefill_kernel", "prefill.cu"
+        # the library runs the tcgen05 prefill kernel for head_dim 64/128,
+        # pages of at least 8 rows and GQA groups up to 16, else the mma.sync one
+        g = w.num_q_heads // w.num_kv_heads
+        if w.head_dim in (64, 128) and w.page_size >= 8 and g <= 16:
+            kernel, kfile = "prefill_tc_kernel", "prefill_tc.cu"
+        else:
+            kernel, kfile = "prefill_kernel", "prefill.cu"
         achieved = work["prefill"]["flops"] / (pf_avg * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1),
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
