@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.num_q_heads / p.num_kv_heads;
   const int P = p.page_size;
+  if (hdr[kHdrNumDecode] == 0) return;  // a prefill-only batch: nothing to set up
 
   // zero both query slots (rows >= G stay zero), init barriers
   for (int i = tid; i < 2 * C::kQBytes / 16; i += kThreads)

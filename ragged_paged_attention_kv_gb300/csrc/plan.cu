@@ -15,30 +15,38 @@ namespace rpa {
 
 constexpr int kPlanThreads = 1024;
 
-// Block-wide exclusive scan of one int per thread; returns the prefix and
-// writes the block total to *total.  All threads of the block must call it.
-__device__ int block_exclusive_scan(int v, int* total, int* smem /* 33 ints */) {
+// Block-wide exclusive scan of two ints per thread (one set of barriers for
+// both); returns the prefixes and writes the block totals to *total.  All
+// threads of the block must call it.
+__device__ int2 block_exclusive_scan2(int2 v, int2* total, int2* smem /* 33 int2 */) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  int2 x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const int yx = __shfl_up_sync(0xffffffffu, x.x, o), yy = __shfl_up_sync(0xffffffffu, x.y, o);
+    if (lane >= o) {
+      x.x += yx;
+      x.y += yy;
+    }
   }
   if (lane == 31) smem[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < (int)(blockDim.x >> 5) ? smem[lane] : 0;
+    int2 w = lane < (int)(blockDim.x >> 5) ? smem[lane] : make_int2(0, 0);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+      const int yx = __shfl_up_sync(0xffffffffu, w.x, o), yy = __shfl_up_sync(0xffffffffu, w.y, o);
+      if (lane >= o) {
+        w.x += yx;
+        w.y += yy;
+      }
     }
     smem[lane] = w;  // inclusive prefix over warps
     if (lane == 31) smem[32] = w;
   }
   __syncthreads();
-  const int excl = x - v + (warp > 0 ? smem[warp - 1] : 0);
+  const int2 before = warp > 0 ? smem[warp - 1] : make_int2(0, 0);
+  const int2 excl = make_int2(x.x - v.x + before.x, x.y - v.y + before.y);
   *total = smem[32];
   __syncthreads();
   return excl;
@@ -60,11 +68,18 @@ struct SeqPlan {
   int flags;      // RPA_STATUS_* bits raised by this sequence
 };
 
-__device__ SeqPlan classify(const rpa_params_t& p, int s, int d0, const int32_t* kv_lens,
-                            const int32_t* qsl) {
+// Sequence s's metadata: query_start_loc[s], [s + 1] and kv_lens[s].
+struct SeqMeta {
+  int a, b, kv;
+};
+__device__ __forceinline__ SeqMeta load_meta(int s, const int32_t* kv_lens, const int32_t* qsl) {
+  return SeqMeta{__ldg(qsl + s), __ldg(qsl + s + 1), __ldg(kv_lens + s)};
+}
+
+__device__ SeqPlan classify(const rpa_params_t& p, int s, int d0, const SeqMeta& m) {
   SeqPlan sp{0, 0, 0, 0, 0, 0};
-  const int a = qsl[s], b = qsl[s + 1];
-  const int kv = kv_lens[s];
+  const int a = m.a, b = m.b;
+  const int kv = m.kv;
   if (a < 0 || b < a || b > p.total_tokens) {
     sp.flags = RPA_STATUS_BAD_QUERY_START_LOC;
     return sp;
@@ -93,7 +108,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
                                                             const int32_t* dist, int32_t* ws,
                                                             int prefill_rows) {
   __shared__ int s_flags;
-  __shared__ int s_scan[33];
+  __shared__ int2 s_scan[33];
   __shared__ unsigned long long s_keys;
   __shared__ int s_doff[kPlanThreads], s_poff[kPlanThreads], s_nsplit[kPlanThreads],
       s_ntiles[kPlanThreads], s_lo[kPlanThreads], s_len[kPlanThreads];
@@ -106,6 +121,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   const int Hkv = p.num_kv_heads, G = p.num_q_heads / p.num_kv_heads;
   const int tile_tokens = prefill_rows / G;  // new tokens per prefill tile
 
+  // the first batch's metadata is loaded together with the distribution
+  // (every index below max_num_seqs is inside the arrays)
+  SeqMeta meta0{0, 0, 0};
+  if (tid < p.max_num_seqs) meta0 = load_meta(tid, kv_lens, qsl);
   if (tid == 0) {
     s_flags = 0;
     s_keys = 0ull;
@@ -117,12 +136,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
     if (tid == 0) atomicOr(&s_flags, RPA_STATUS_BAD_DISTRIBUTION);
     S = 0;
   }
-  if (tid == 0 && S > 0 && qsl[0] != 0) atomicOr(&s_flags, RPA_STATUS_BAD_QUERY_START_LOC);
+  if (tid == 0 && S > 0 && meta0.a != 0) atomicOr(&s_flags, RPA_STATUS_BAD_QUERY_START_LOC);
 
   // Pass 1: total decode keys (per kv head) to size the splits.
   unsigned long long my_keys = 0;
   for (int s = tid; s < S; s += kPlanThreads) {
-    SeqPlan sp = classify(p, s, d0, kv_lens, qsl);
+    SeqPlan sp = classify(p, s, d0, s == tid ? meta0 : load_meta(s, kv_lens, qsl));
     if (sp.flags) atomicOr(&s_flags, sp.flags);
     if (sp.cls == 1) my_keys += (unsigned long long)(sp.kv_len - sp.lo);
   }
@@ -148,13 +167,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
     SeqPlan sp{0, 0, 0, 0, 0, 0};
     int nsplit = 0, ntiles = 0;
     if (s < S) {
-      sp = classify(p, s, d0, kv_lens, qsl);  // flags were taken in pass 1
+      // flags were taken in pass 1
+      sp = classify(p, s, d0, s == tid ? meta0 : load_meta(s, kv_lens, qsl));
       if (sp.cls == 1) nsplit = (sp.kv_len - (sp.lo & ~63) + chunk - 1) / chunk;
       if (sp.cls == 2) ntiles = (sp.q_len + tile_tokens - 1) / tile_tokens;
     }
-    int dec_total, pf_total;
-    const int dec_off = block_exclusive_scan(nsplit * Hkv, &dec_total, s_scan);
-    const int pf_off = block_exclusive_scan(ntiles * Hkv, &pf_total, s_scan);
+    int2 totals;
+    const int2 offs = block_exclusive_scan2(make_int2(nsplit * Hkv, ntiles * Hkv), &totals, s_scan);
+    const int dec_off = offs.x, pf_off = offs.y, dec_total = totals.x, pf_total = totals.y;
     s_doff[tid] = dec_off;
     s_poff[tid] = pf_off;
     s_nsplit[tid] = nsplit;

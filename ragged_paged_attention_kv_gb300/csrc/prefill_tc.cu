@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int P = p.page_size;
   const int W = p.sliding_window;
   const int n_units = hdr[kHdrNumPrefill];
+  if (n_units == 0) return;  // a decode-only batch: nothing to set up
 
   if (tid == 0) {
     s_abort = 0;
