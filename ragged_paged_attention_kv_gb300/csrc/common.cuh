@@ -25,9 +25,12 @@ enum HeaderWord {
 };
 
 // Decode unit: one (sequence, kv head, key split).
+// Decode unit: one (sequence, kv head, split of the key range).  The units of
+// one (seq, head) are contiguous, so split 0 of unit u is unit u - split.  The
+// sequence's token row q0 and kv_len ride along, so one load gives a unit.
 struct DecodeUnit {
-  int32_t seq, head, k_begin, k_end;    // keys [k_begin, k_end) of this split
-  int32_t split, nsplit, first_unit, pad;  // units of one (seq, head) are contiguous
+  int32_t seq, head, k_begin, k_end;  // keys [k_begin, k_end) of this split
+  int32_t split, nsplit, q0, kv_len;
 };
 
 // Prefill unit: one (sequence, tile of new tokens, kv head).

@@ -60,9 +60,9 @@ struct Cfg {
 
 // What the producer tells the consumers about the unit in a query slot.
 struct UnitInfo {
-  DecodeUnit du;  // du.pad holds the unit's index; du.seq < 0 means "no more units"
+  DecodeUnit du;  // du.seq < 0 means "no more units"
   int q0, ctx;    // the sequence's token row and the new token's position
-  int pad[6];
+  int pad[6];     // pad[0]: the unit's index (its partial results live there)
 };
 static_assert(sizeof(UnitInfo) == 64, "two UnitInfo slots take 128 bytes");
 
@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int q0 = 0, kv_len = 0;
       if (u < n_units) {
         du = units[u];
-        q0 = a.qsl[du.seq];
-        kv_len = a.kv_lens[du.seq];
+        q0 = du.q0;
+        kv_len = du.kv_len;
       }
       const int kb0 = du.k_begin & ~(kBN - 1);
       const int n_st = u < n_units ? (du.k_end - kb0 + kBN - 1) / kBN : 0;
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         UnitInfo ui;
         ui.du = du;
-        ui.du.pad = u;  // consumers need the unit's index for its partial results
+        ui.pad[0] = u;
         ui.q0 = q0;
         ui.ctx = kv_len - 1;
         info[slot] = ui;
@@ -244,9 +244,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const DecodeUnit du = info[slot].du;
     if (du.seq < 0) break;
+    const int u_idx = info[slot].pad[0];  // read now: the slot is refilled once Q is taken
     const int seq = du.seq, h = du.head;
     const int q0 = info[slot].q0;
     const int ctx = info[slot].ctx;
+    // split 0 stores the new token's key/value into its page after the
+    // stages; the page id and the inputs are loaded now so that store does
+    // not wait for them
+    TokenKvLane tkv{};
+    if (du.split == 0 && warp == 0) tkv = token_kv_load<FP8>(a.kv, seq, q0, ctx, h, lane);
 
     uint32_t qa[D / 16][4];
     {
@@ -426,8 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       break;
     }
 
-    // split 0 stores the new token's key/value into its page
-    if (du.split == 0 && warp == 0) write_token_kv<FP8>(a.kv, seq, q0, ctx, h, lane);
+    if (du.split == 0 && warp == 0) token_kv_store<FP8>(a.kv, tkv, ctx, h, lane);
 
     // per-warp state -> shared memory rows [warp][16] of (m, l, O[D])
     {
@@ -483,10 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
         *reinterpret_cast<uint2*>(dst) = pk;
       } else {
-        const int u = du.pad;  // this unit's index (set by the producer)
-        float* po = part_o + ((int64_t)u * G + r) * D + d;
+        float* po = part_o + ((int64_t)u_idx * G + r) * D + d;
         *reinterpret_cast<float4*>(po) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        if (d == 0) part_ml[(int64_t)u * G + r] = make_float2(M, Lsum);
+        if (d == 0) part_ml[(int64_t)u_idx * G + r] = make_float2(M, Lsum);
       }
     }
 
@@ -508,11 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int hq = h * G + r;
           float M = a.sink ? a.sink[hq] * kLog2e : -INFINITY;
           for (int k = 0; k < du.nsplit; ++k)
-            M = fmaxf(M, __ldcg(&part_ml[(int64_t)(du.first_unit + k) * G + r].x));
+            M = fmaxf(M, __ldcg(&part_ml[(int64_t)(u_idx - du.split + k) * G + r].x));
           float Lsum = a.sink ? exp2f(a.sink[hq] * kLog2e - M) : 0.f;
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
           for (int k = 0; k < du.nsplit; ++k) {
-            const int64_t pu = (int64_t)(du.first_unit + k) * G + r;
+            const int64_t pu = (int64_t)(u_idx - du.split + k) * G + r;
             const float2 ml = __ldcg(&part_ml[pu]);
             const float scs = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
             Lsum += scs * ml.y;

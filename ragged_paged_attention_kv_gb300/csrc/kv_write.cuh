@@ -59,6 +59,46 @@ __device__ __forceinline__ void write_token_kv(const KvArgs& a, int seq, int t, 
   }
 }
 
+// The same write for one token split into its two halves, so that a caller
+// can issue the page-id and input loads early and store later: lane l holds
+// 16-byte chunk l of the token's key row then value row (head_dim <= 128).
+// Nothing reads the loaded values before token_kv_store, so the loads do
+// not stall the caller in between.
+struct TokenKvLane {
+  int32_t page;  // block-table entry of the token's slot
+  uint4 x;       // the chunk's bf16 input
+};
+template <bool FP8>
+__device__ __forceinline__ TokenKvLane token_kv_load(const KvArgs& a, int seq, int t, int pos,
+                                                     int h, int lane) {
+  TokenKvLane r{0, make_uint4(0, 0, 0, 0)};
+  const int D = a.p.head_dim;
+  const int chunks = D / 8;
+  if (lane >= 2 * chunks) return r;
+  const int kv = lane / chunks, c = lane % chunks;
+  r.page = __ldg(a.block_tables + (int64_t)seq * a.p.pages_per_seq + pos / a.p.page_size);
+  r.x = __ldg(reinterpret_cast<const uint4*>((kv ? a.values : a.keys) +
+                                             ((int64_t)t * a.p.num_kv_heads + h) * D + c * 8));
+  return r;
+}
+template <bool FP8>
+__device__ __forceinline__ void token_kv_store(const KvArgs& a, const TokenKvLane& r, int pos,
+                                               int h, int lane) {
+  const int chunks = a.p.head_dim / 8;
+  if (lane >= 2 * chunks) return;
+  if (r.page < 0 || r.page >= a.p.num_pages) {
+    set_status(a.ws, RPA_STATUS_BAD_PAGE);
+    return;
+  }
+  const int kv = lane / chunks, c = lane % chunks;
+  const int64_t dst = pool_offset(a.p, r.page, pos % a.p.page_size, 2 * h + kv, FP8 ? 1 : 2);
+  if (FP8)
+    *reinterpret_cast<uint2*>(a.cache + dst + c * 8) =
+        quantize8(r.x, kv ? a.p.v_scale : a.p.k_scale);
+  else
+    *reinterpret_cast<uint4*>(a.cache + dst + c * 16) = r.x;
+}
+
 // One warp writes key and value head `h` of the n consecutive input tokens
 // t0 .. t0+n-1 (positions pos0 .. pos0+n-1 of sequence `seq`) into the pool.
 // Lanes take consecutive 16-byte chunks (a token's key row, then its value

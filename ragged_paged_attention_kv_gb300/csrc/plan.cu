@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   __shared__ int2 s_scan[33];
   __shared__ unsigned long long s_keys;
   __shared__ int s_doff[kPlanThreads], s_poff[kPlanThreads], s_nsplit[kPlanThreads],
-      s_ntiles[kPlanThreads], s_lo[kPlanThreads], s_len[kPlanThreads];
+      s_ntiles[kPlanThreads], s_lo[kPlanThreads], s_len[kPlanThreads], s_q0[kPlanThreads];
   const WorkspaceLayout L(p);
   DecodeUnit* dunits = reinterpret_cast<DecodeUnit*>(reinterpret_cast<char*>(ws) + L.decode_units_off);
   PrefillUnit* punits =
@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
     s_ntiles[tid] = ntiles;
     s_lo[tid] = sp.lo;
     s_len[tid] = sp.cls == 1 ? sp.kv_len : sp.q_len;
+    s_q0[tid] = sp.q0;
     __syncthreads();
     for (int u = tid; u < dec_total; u += kPlanThreads) {
       const int i = last_at_or_below(s_doff, kPlanThreads, u);
@@ -195,8 +196,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
       du.k_end = min(kv, stage0 + (k + 1) * chunk);
       du.split = k;
       du.nsplit = ns;
-      du.first_unit = dec_base + s_doff[i] + h * ns;
-      du.pad = 0;
+      du.q0 = s_q0[i];
+      du.kv_len = kv;
       dunits[dec_base + u] = du;
       if (k == 0) counters[(int64_t)(base + i) * Hkv + h] = 0;
     }
