@@ -434,23 +434,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (du.split == 0 && warp == 0) token_kv_store<FP8>(a.kv, tkv, ctx, h, lane);
 
-    // per-warp state -> shared memory rows [warp][16] of (m, l, O[D])
+    // per-warp state -> shared memory rows [warp][row] of (m, l, O[D]); only
+    // the G rows of the GQA group are real, the rest of the 16-row tile is
+    // padding and is not stored
     {
       float* mw = sMerge + warp * kDecodeRows * (D + 2);
       const float l0 = quad_sum(l_run[0]), l1 = quad_sum(l_run[1]);
-      if (tq == 0) {
-        mw[gq * (D + 2) + 0] = m_run[0];
-        mw[gq * (D + 2) + 1] = l0;
-        mw[(gq + 8) * (D + 2) + 0] = m_run[1];
-        mw[(gq + 8) * (D + 2) + 1] = l1;
-      }
+      if (gq < G) {
+        float* row = mw + gq * (D + 2);
+        if (tq == 0) *reinterpret_cast<float2*>(row) = make_float2(m_run[0], l0);
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        const int d = n * 8 + 2 * tq;
-        mw[gq * (D + 2) + 2 + d] = o[n][0];
-        mw[gq * (D + 2) + 2 + d + 1] = o[n][1];
-        mw[(gq + 8) * (D + 2) + 2 + d] = o[n][2];
-        mw[(gq + 8) * (D + 2) + 2 + d + 1] = o[n][3];
+        for (int n = 0; n < D / 8; ++n)
+          *reinterpret_cast<float2*>(row + 2 + n * 8 + 2 * tq) = make_float2(o[n][0], o[n][1]);
+      }
+      if (gq + 8 < G) {
+        float* row = mw + (gq + 8) * (D + 2);
+        if (tq == 0) *reinterpret_cast<float2*>(row) = make_float2(m_run[1], l1);
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n)
+          *reinterpret_cast<float2*>(row + 2 + n * 8 + 2 * tq) = make_float2(o[n][2], o[n][3]);
       }
     }
     named_bar(1, kConsumerWarps * 32);
