@@ -42,7 +42,9 @@
  *   attention_sink [Hq] fp32 or NULL.
  *   out          [T, Hq, D] bf16; rows >= qsl[S] are left untouched.
  *
- * Semantics (per sequence s, new token i, q-head hq, kv head h = hq/(Hq/Hkv)):
+ * Semantics (per sequence s, new token i, q-head hq, kv head h = hq/(Hq/Hkv);
+ * k_scale and v_scale below are those of head h when per-head scales are
+ * given):
  *   position p = kv_len - q_len + i; keys j with j <= p and, when
  *   sliding_window W > 0, p - j < W (vLLM's window_size = (W-1, 0));
  *   logit = softmax_scale * k_scale * (q . k_j), then cap*tanh(logit/cap) when
@@ -72,7 +74,8 @@ extern "C" {
 
 /* Return codes of every entry point. */
 #define RPA_OK 0
-#define RPA_ERR_INVALID_ARG 1  /* null pointer, negative size, bad scale   */
+#define RPA_ERR_INVALID_ARG 1  /* null pointer, negative size, bad scale,
+                                  per-head scales with a bf16 cache        */
 #define RPA_ERR_UNSUPPORTED 2  /* head_dim not 64/128, Hq/Hkv not in {1,2,4,8,16},
                                   page_size not a power of two in [1,1024] */
 #define RPA_ERR_WORKSPACE 3    /* workspace NULL, misaligned or too small   */
@@ -86,6 +89,7 @@ extern "C" {
 #define RPA_STATUS_DECODE_QLEN 0x10      /* a decode-class sequence with q_len != 1
                                             (informational: it is still computed) */
 #define RPA_STATUS_TIMEOUT 0x20          /* a bounded device wait gave up */
+#define RPA_STATUS_BAD_SCALE 0x40        /* a per-head scale not finite and > 0 */
 
 typedef enum { RPA_KV_BF16 = 0, RPA_KV_FP8_E4M3 = 1 } rpa_kv_dtype_t;
 
@@ -104,6 +108,16 @@ typedef struct {
   float logits_soft_cap;  /* > 0 enables cap*tanh(x/cap); 0 = none          */
   float k_scale;          /* fp8: dequantisation scales; bf16: must be 1    */
   float v_scale;
+  /* Optional per-kv-head scales (fp8 caches only), device arrays of
+   * num_kv_heads fp32, 4-byte aligned, read by the kernels: when non-NULL,
+   * k_scale_heads[h] (v_scale_heads[h]) replaces k_scale (v_scale) for kv
+   * head h in the quantisation of the new keys (values), in the logits and
+   * in the output.  Each must be finite and > 0: otherwise the call sets
+   * RPA_STATUS_BAD_SCALE and that head's outputs and pages are unspecified.
+   * NULL for bf16 caches.  (vLLM's fp8 caches use one scale per layer; one
+   * per kv head is the finer variant.) */
+  const float* k_scale_heads;
+  const float* v_scale_heads;
 } rpa_params_t;
 
 /* Bytes of device workspace rpa_forward / rpa_update_cache need for these

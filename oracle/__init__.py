@@ -51,6 +51,8 @@ class OracleParams(ctypes.Structure):
         ("logits_soft_cap", ctypes.c_double),
         ("k_scale", ctypes.c_double),
         ("v_scale", ctypes.c_double),
+        ("k_scale_heads", ctypes.POINTER(ctypes.c_double)),
+        ("v_scale_heads", ctypes.POINTER(ctypes.c_double)),
     ]
 
 
@@ -119,14 +121,29 @@ def max_threads() -> int:
 def make_params(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                 pages_per_seq, max_num_seqs, total_tokens, kv_fp8=False,
                 sliding_window=0, softmax_scale=1.0, logits_soft_cap=0.0,
-                k_scale=1.0, v_scale=1.0) -> OracleParams:
-    """Scales are fp32 numbers in the interface; they are rounded to fp32 here."""
+                k_scale=1.0, v_scale=1.0, k_scale_heads=None, v_scale_heads=None) -> OracleParams:
+    """Scales are fp32 numbers in the interface; they are rounded to fp32 here.
+    ``k_scale_heads`` / ``v_scale_heads``: optional per-kv-head scales (fp8)."""
     f32 = lambda x: float(np.float32(x))
-    return OracleParams(int(num_q_heads), int(num_kv_heads), int(head_dim),
-                        int(page_size), int(num_pages), int(pages_per_seq),
-                        int(max_num_seqs), int(total_tokens), int(bool(kv_fp8)),
-                        int(sliding_window or 0), f32(softmax_scale),
-                        f32(logits_soft_cap or 0.0), f32(k_scale), f32(v_scale))
+
+    def heads(x):
+        if x is None:
+            return None, None
+        a = np.asarray(x, dtype=np.float32).astype(np.float64)
+        if a.shape != (int(num_kv_heads),):
+            raise ValueError("per-head scales need num_kv_heads entries")
+        a = np.ascontiguousarray(a)
+        return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+    kh, kp = heads(k_scale_heads)
+    vh, vp = heads(v_scale_heads)
+    p = OracleParams(int(num_q_heads), int(num_kv_heads), int(head_dim),
+                     int(page_size), int(num_pages), int(pages_per_seq),
+                     int(max_num_seqs), int(total_tokens), int(bool(kv_fp8)),
+                     int(sliding_window or 0), f32(softmax_scale),
+                     f32(logits_soft_cap or 0.0), f32(k_scale), f32(v_scale), kp, vp)
+    p._keep = (kh, vh)  # the arrays must live as long as the params
+    return p
 
 
 def _c(a, dtype):

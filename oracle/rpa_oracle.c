@@ -28,7 +28,9 @@
  *
  *   - oracle_attention_rows: exact softmax attention per (token, q-head):
  *     GQA head map h = hq / (Hq/Hkv); score s_j = softmax_scale * (q . k_j)
- *     (k_j dequantised with k_scale for fp8); optional soft cap
+ *     (k_j dequantised with k_scale for fp8 -- or, when per-head scales
+ *     are given, with the scale of kv head h; likewise v_scale); optional
+ *     soft cap
  *     s = cap * tanh(s / cap); causal mask j <= pos; sliding window keeps
  *     pos - j < W (vLLM's window_size = (W-1, 0)); an optional per-q-head
  *     sink logit joins the softmax denominator with no value vector
@@ -62,7 +64,17 @@ typedef struct {
   double logits_soft_cap;  /* 0: none                                     */
   double k_scale;          /* fp8 only; the values are fp32 numbers       */
   double v_scale;
+  const double* k_scale_heads;  /* fp8 only, optional: [num_kv_heads] scales  */
+  const double* v_scale_heads;  /* that replace k_scale / v_scale per head   */
 } oracle_params;
+
+/* The key / value scale of kv head h. */
+static double key_scale(const oracle_params* p, int h) {
+  return p->k_scale_heads ? p->k_scale_heads[h] : p->k_scale;
+}
+static double value_scale(const oracle_params* p, int h) {
+  return p->v_scale_heads ? p->v_scale_heads[h] : p->v_scale;
+}
 
 enum {
   ORACLE_OK = 0,
@@ -140,6 +152,9 @@ static int check_params(const oracle_params* p) {
   if (p->sliding_window < 0 || p->logits_soft_cap < 0.0) return ORACLE_BAD_ARG;
   if (p->kv_fp8 && (!(p->k_scale > 0.0) || !(p->v_scale > 0.0)))
     return ORACLE_BAD_ARG;
+  if (!p->kv_fp8 && (p->k_scale_heads || p->v_scale_heads)) return ORACLE_BAD_ARG;
+  for (int h = 0; h < p->num_kv_heads; ++h)
+    if (!(key_scale(p, h) > 0.0) || !(value_scale(p, h) > 0.0)) return ORACLE_BAD_ARG;
   return ORACLE_OK;
 }
 
@@ -233,8 +248,8 @@ int oracle_update_cache(const oracle_params* p, const uint16_t* keys,
         int64_t ov = cache_offset(p, page, row, 2 * h + 1);
         for (int d = 0; d < D; ++d) {
           if (p->kv_fp8) {
-            kv_cache[ok + d] = oracle_quantize(k[d], p->k_scale);
-            kv_cache[ov + d] = oracle_quantize(v[d], p->v_scale);
+            kv_cache[ok + d] = oracle_quantize(k[d], key_scale(p, h));
+            kv_cache[ov + d] = oracle_quantize(v[d], value_scale(p, h));
           } else {
             memcpy(kv_cache + ok + 2 * (int64_t)d, &k[d], 2);
             memcpy(kv_cache + ov + 2 * (int64_t)d, &v[d], 2);
@@ -307,7 +322,7 @@ int oracle_attention_rows(const oracle_params* p, const uint16_t* queries,
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
           dot += oracle_bf16_to_double(q[d]) *
-                 cache_value(p, kv_cache, off, d, p->k_scale);
+                 cache_value(p, kv_cache, off, d, key_scale(p, h));
         double sc = p->softmax_scale * dot;
         if (p->logits_soft_cap > 0.0)
           sc = p->logits_soft_cap * tanh(sc / p->logits_soft_cap);
@@ -329,7 +344,7 @@ int oracle_attention_rows(const oracle_params* p, const uint16_t* queries,
         int64_t off = cache_offset(p, page_of(p, block_tables, s, j),
                                    j % p->page_size, 2 * h + 1);
         for (int d = 0; d < D; ++d)
-          o[d] += e * cache_value(p, kv_cache, off, d, p->v_scale);
+          o[d] += e * cache_value(p, kv_cache, off, d, value_scale(p, h));
       }
       for (int d = 0; d < D; ++d) o[d] /= den;
     }

@@ -11,7 +11,8 @@ fallback.
                   softmax_scale=..., sliding_window=None, logits_soft_cap=None,
                   k_scale=None, v_scale=None)
 
-The argument list follows the ejkernel ``ragged_page_attention_v3``
+``k_scale`` / ``v_scale`` are numbers, or (fp8 caches) float32 device tensors
+of num_kv_heads entries for one scale per kv head.  The argument list follows the ejkernel ``ragged_page_attention_v3``
 interface; ``kv_cache`` is updated in place (the new keys/values are written
 into their pages) instead of being returned.
 """
@@ -31,13 +32,19 @@ __all__ = ["make_params", "workspace_size", "alloc_workspace", "forward", "updat
 
 def make_params(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, pages_per_seq,
                 max_num_seqs, total_tokens, kv_fp8=False, sliding_window=None,
-                softmax_scale=1.0, logits_soft_cap=None, k_scale=None, v_scale=None) -> RpaParams:
+                softmax_scale=1.0, logits_soft_cap=None, k_scale=None, v_scale=None,
+                k_scale_heads=None, v_scale_heads=None) -> RpaParams:
+    """``k_scale_heads`` / ``v_scale_heads``: optional float32 device tensors of
+    num_kv_heads per-head scales (fp8 caches); they must outlive the calls
+    that use these params."""
     return RpaParams(int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size),
                      int(num_pages), int(pages_per_seq), int(max_num_seqs), int(total_tokens),
                      _lib.RPA_KV_FP8_E4M3 if kv_fp8 else _lib.RPA_KV_BF16,
                      int(sliding_window or 0), float(softmax_scale), float(logits_soft_cap or 0.0),
                      float(1.0 if k_scale is None else k_scale),
-                     float(1.0 if v_scale is None else v_scale))
+                     float(1.0 if v_scale is None else v_scale),
+                     None if k_scale_heads is None else k_scale_heads.data_ptr(),
+                     None if v_scale_heads is None else v_scale_heads.data_ptr())
 
 
 def workspace_size(params: RpaParams) -> int:
@@ -75,9 +82,21 @@ def _stream(stream, device):
 _FP8_TYPES = (torch.uint8, torch.float8_e4m3fn)
 
 
+def _scale_arg(x, name, Hkv, device):
+    """(scalar, per-head tensor or None) for a k_scale / v_scale argument."""
+    if isinstance(x, torch.Tensor):
+        _need(x, name, (torch.float32,), device)
+        if x.numel() != Hkv:
+            raise ValueError(f"{name} as a tensor must have num_kv_heads entries")
+        return 1.0, x
+    return x, None
+
+
 def _params_from(queries_or_none, keys, kv_cache, kv_lens, block_tables, softmax_scale,
                  sliding_window, logits_soft_cap, k_scale, v_scale, num_q_heads=None):
     T, Hkv, D = keys.shape
+    k_scale, k_heads = _scale_arg(k_scale, "k_scale", Hkv, keys.device)
+    v_scale, v_heads = _scale_arg(v_scale, "v_scale", Hkv, keys.device)
     num_pages, P, C, D2 = kv_cache.shape
     if C != 2 * Hkv or D2 != D:
         raise ValueError("kv_cache must be [num_pages, page_size, 2*num_kv_heads, head_dim]")
@@ -90,7 +109,8 @@ def _params_from(queries_or_none, keys, kv_cache, kv_lens, block_tables, softmax
                        num_pages=num_pages, pages_per_seq=block_tables.numel() // max_num_seqs,
                        max_num_seqs=max_num_seqs, total_tokens=T, kv_fp8=fp8,
                        sliding_window=sliding_window, softmax_scale=softmax_scale,
-                       logits_soft_cap=logits_soft_cap, k_scale=k_scale, v_scale=v_scale)
+                       logits_soft_cap=logits_soft_cap, k_scale=k_scale, v_scale=v_scale,
+                       k_scale_heads=k_heads, v_scale_heads=v_heads)
 
 
 def forward(queries, keys, values, kv_cache, kv_lens, block_tables, query_start_loc,

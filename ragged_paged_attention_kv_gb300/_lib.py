@@ -24,6 +24,7 @@ RPA_STATUS_BAD_QUERY_START_LOC = 0x4
 RPA_STATUS_BAD_DISTRIBUTION = 0x8
 RPA_STATUS_DECODE_QLEN = 0x10
 RPA_STATUS_TIMEOUT = 0x20
+RPA_STATUS_BAD_SCALE = 0x40
 
 RPA_KV_BF16 = 0
 RPA_KV_FP8_E4M3 = 1
@@ -50,6 +51,8 @@ class RpaParams(ctypes.Structure):
         ("logits_soft_cap", ctypes.c_float),
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
+        ("k_scale_heads", ctypes.c_void_p),
+        ("v_scale_heads", ctypes.c_void_p),
     ]
 
 

@@ -32,7 +32,10 @@ static int check_params(const rpa_params_t* p) {
     return RPA_ERR_INVALID_ARG;
   if (p->kv_dtype == RPA_KV_FP8_E4M3) {
     if (!(p->k_scale > 0.f) || !(p->v_scale > 0.f)) return RPA_ERR_INVALID_ARG;
-  } else if (p->k_scale != 1.f || p->v_scale != 1.f) {
+    if ((reinterpret_cast<uintptr_t>(p->k_scale_heads) & 3) != 0 ||
+        (reinterpret_cast<uintptr_t>(p->v_scale_heads) & 3) != 0)
+      return RPA_ERR_INVALID_ARG;
+  } else if (p->k_scale != 1.f || p->v_scale != 1.f || p->k_scale_heads || p->v_scale_heads) {
     return RPA_ERR_INVALID_ARG;
   }
   // pool byte offsets and token rows must stay inside int64 / int32 ranges

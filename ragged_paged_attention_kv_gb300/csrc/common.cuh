@@ -239,17 +239,22 @@ __device__ __forceinline__ float tanh_exp(float x) {
 }
 
 // Logit transform shared by the kernels: raw dot product -> log2-domain
-// logit.  scale_log2 = softmax_scale * k_scale * log2(e); with a soft cap,
-// cap * tanh(x / cap) is applied to the natural-domain logit first.
+// logit; with a soft cap, cap * tanh(x / cap) is applied to the
+// natural-domain logit x = softmax_scale * k_scale * dot first.  Two numbers
+// per kv head: with a soft cap, cap * log2e * tanh(dot * mul) with mul =
+// softmax_scale * k_scale / cap; without, dot * mul with mul = softmax_scale
+// * k_scale * log2e.
 struct LogitXform {
-  float scale_nat;   // softmax_scale * k_scale
-  float cap;         // 0 = none
-  float inv_cap;
-  float scale_log2;  // scale_nat * log2e (no cap)
+  float mul;
+  float cap2;  // cap * log2e, 0 = no cap
   __device__ __forceinline__ float operator()(float dot) const {
-    if (cap > 0.f) return cap * tanh_exp(dot * scale_nat * inv_cap) * kLog2e;
-    return dot * scale_log2;
+    if (cap2 > 0.f) return cap2 * tanh_exp(dot * mul);
+    return dot * mul;
   }
 };
+__device__ __forceinline__ LogitXform make_xform(float softmax_scale, float k_scale, float cap) {
+  return cap > 0.f ? LogitXform{softmax_scale * k_scale / cap, cap * kLog2e}
+                   : LogitXform{softmax_scale * k_scale * kLog2e, 0.f};
+}
 
 }  // namespace rpa

@@ -231,9 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // -------------------------------------------------------------- consumers
   const int gq = lane >> 2, tq = lane & 3;
-  const LogitXform xf{p.softmax_scale * p.k_scale, p.logits_soft_cap,
-                      p.logits_soft_cap > 0.f ? 1.f / p.logits_soft_cap : 0.f,
-                      p.softmax_scale * p.k_scale * kLog2e};
   uint32_t g = 0;
   for (uint32_t uq = 0;; ++uq) {
     const int slot = uq & 1;
@@ -248,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seq = du.seq, h = du.head;
     const int q0 = info[slot].q0;
     const int ctx = info[slot].ctx;
+    const float ks = k_scale_of(p, h), vs = v_scale_of(p, h);  // this kv head's scales
+    const LogitXform xf = make_xform(p.softmax_scale, ks, p.logits_soft_cap);
     // split 0 stores the new token's key/value into its page after the
     // stages; the page id and the inputs are loaded now so that store does
     // not wait for them
@@ -306,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __nv_bfloat16* in = (kv ? a.kv.values : a.kv.keys) +
                                       ((int64_t)q0 * p.num_kv_heads + h) * D + c * 8;
             val = dequant8(quantize8(__ldg(reinterpret_cast<const uint4*>(in)),
-                                     kv ? p.v_scale : p.k_scale));
+                                     kv ? vs : ks));
           } else {
             const uint2 codes = *reinterpret_cast<const uint2*>(
                 smem + (stage - s_base) + (2 * (warp * kKeysPerWarp + r) + kv) * C::kRowBytes + c * 8);
@@ -483,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[e] *= scs;
         }
-        const float inv = p.v_scale / Lsum;
+        const float inv = vs / Lsum;
         __nv_bfloat16* dst = a.out + ((int64_t)q0 * p.num_q_heads + hq) * D + d;
         uint2 pk;
         pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
@@ -528,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc[2] += scs * po.z;
             acc[3] += scs * po.w;
           }
-          const float inv = p.v_scale / Lsum;
+          const float inv = vs / Lsum;
           __nv_bfloat16* dst = a.out + ((int64_t)q0 * p.num_q_heads + hq) * D + d;
           uint2 pk;
           pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);

@@ -16,6 +16,14 @@ struct KvArgs {
   int32_t* ws;                  // workspace header
 };
 
+// Scales of kv head h: the per-head arrays when given, else the scalars.
+__device__ __forceinline__ float k_scale_of(const rpa_params_t& p, int h) {
+  return p.k_scale_heads ? __ldg(p.k_scale_heads + h) : p.k_scale;
+}
+__device__ __forceinline__ float v_scale_of(const rpa_params_t& p, int h) {
+  return p.v_scale_heads ? __ldg(p.v_scale_heads + h) : p.v_scale;
+}
+
 // Physical page of logical position `pos` of sequence `seq`, or -1 (and the
 // BAD_PAGE status bit) if the table entry lies outside the pool.
 __device__ __forceinline__ int32_t lookup_page(const KvArgs& a, int seq, int pos) {
@@ -51,7 +59,7 @@ __device__ __forceinline__ void write_token_kv(const KvArgs& a, int seq, int t, 
     const __nv_bfloat16* in = (kv ? a.values : a.keys) + src + c * 8;
     const uint4 x = __ldg(reinterpret_cast<const uint4*>(in));
     if (FP8) {
-      const float scale = kv ? a.p.v_scale : a.p.k_scale;
+      const float scale = kv ? v_scale_of(a.p, h) : k_scale_of(a.p, h);
       *reinterpret_cast<uint2*>(a.cache + dst + (int64_t)kv * D + c * 8) = quantize8(x, scale);
     } else {
       *reinterpret_cast<uint4*>(a.cache + dst + ((int64_t)kv * D + c * 8) * 2) = x;
@@ -94,7 +102,7 @@ __device__ __forceinline__ void token_kv_store(const KvArgs& a, const TokenKvLan
   const int64_t dst = pool_offset(a.p, r.page, pos % a.p.page_size, 2 * h + kv, FP8 ? 1 : 2);
   if (FP8)
     *reinterpret_cast<uint2*>(a.cache + dst + c * 8) =
-        quantize8(r.x, kv ? a.p.v_scale : a.p.k_scale);
+        quantize8(r.x, kv ? v_scale_of(a.p, h) : k_scale_of(a.p, h));
   else
     *reinterpret_cast<uint4*>(a.cache + dst + c * 16) = r.x;
 }
@@ -137,7 +145,7 @@ __device__ __forceinline__ void write_tokens_kv(const KvArgs& a, int seq, int t0
       const int64_t dst = pool_offset(a.p, page[b], pos % a.p.page_size, 2 * h + kv, FP8 ? 1 : 2);
       if (FP8) {
         *reinterpret_cast<uint2*>(a.cache + dst + c * 8) =
-            quantize8(x[b], kv ? a.p.v_scale : a.p.k_scale);
+            quantize8(x[b], kv ? v_scale_of(a.p, h) : k_scale_of(a.p, h));
       } else {
         *reinterpret_cast<uint4*>(a.cache + dst + c * 16) = x[b];
       }

@@ -8,6 +8,8 @@
 // ragged_page_attention_v3 interface's `distribution` argument defines the
 // classes; results never depend on it (a decode-class sequence with
 // q_len != 1 is flagged and planned as a prefill).
+#include <cfloat>
+
 #include "common.cuh"
 #include "kv_write.cuh"
 
@@ -137,6 +139,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
     S = 0;
   }
   if (tid == 0 && S > 0 && meta0.a != 0) atomicOr(&s_flags, RPA_STATUS_BAD_QUERY_START_LOC);
+  // per-head scales must be finite and positive
+  if (p.k_scale_heads || p.v_scale_heads) {
+    for (int h = tid; h < Hkv; h += kPlanThreads) {
+      const float ks = p.k_scale_heads ? __ldg(p.k_scale_heads + h) : 1.f;
+      const float vs = p.v_scale_heads ? __ldg(p.v_scale_heads + h) : 1.f;
+      if (!(ks > 0.f && ks <= FLT_MAX && vs > 0.f && vs <= FLT_MAX))
+        atomicOr(&s_flags, RPA_STATUS_BAD_SCALE);
+    }
+  }
 
   // Pass 1: total decode keys (per kv head) to size the splits.
   unsigned long long my_keys = 0;

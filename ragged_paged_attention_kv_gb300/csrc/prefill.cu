@@ -66,7 +66,7 @@ __device__ __forceinline__ void load_tile(const AttnArgs& a, uint8_t* stage, int
       const __nv_bfloat16* in =
           (kv ? a.kv.values : a.kv.keys) + ((int64_t)(q0 + (j - ctx)) * Hkv + h) * D + c * 8;
       if (FP8) {
-        const float scale = kv ? a.kv.p.v_scale : a.kv.p.k_scale;
+        const float scale = kv ? v_scale_of(a.kv.p, h) : k_scale_of(a.kv.p, h);
         *reinterpret_cast<uint4*>(dst) =
             dequant8(quantize8(__ldg(reinterpret_cast<const uint4*>(in)), scale));
       } else {
@@ -94,9 +94,6 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
   const int G = p.num_q_heads / p.num_kv_heads;
   const int W = p.sliding_window;
   const int n_units = hdr[kHdrNumPrefill];
-  const LogitXform xf{p.softmax_scale * p.k_scale, p.logits_soft_cap,
-                      p.logits_soft_cap > 0.f ? 1.f / p.logits_soft_cap : 0.f,
-                      p.softmax_scale * p.k_scale * kLog2e};
 
   if (tid == 0) s_unit = atomicAdd(hdr + kHdrPrefillNext, 1);
   __syncthreads();
@@ -106,6 +103,8 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
     if (tid == 0) next = atomicAdd(hdr + kHdrPrefillNext, 1);
     const PrefillUnit pu = units[u];
     const int seq = pu.seq, h = pu.head;
+    const float ks = k_scale_of(p, h);  // this kv head's key scale
+    const LogitXform xf = make_xform(p.softmax_scale, ks, p.logits_soft_cap);
     const int q0 = a.qsl[seq];
     const int q_len = a.qsl[seq + 1] - q0;
     const int ctx = a.kv_lens[seq] - q_len;
@@ -270,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
         l = l * sc + exp2f(sk - m2);
       }
       if (ti >= n_tok) continue;
-      const float inv = sc * p.v_scale / l;
+      const float inv = sc * v_scale_of(p, h) / l;
       __nv_bfloat16* dst = a.out + ((int64_t)(q0 + pu.t_begin + ti) * p.num_q_heads + hq) * D;
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) {

@@ -143,7 +143,7 @@ __device__ __forceinline__ UnitGeom unit_geom(const AttnArgs& a, const PrefillUn
   return g;
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PH>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ TcMaps maps, AttnArgs a) {
   using C = TcCfg<D, FP8>;
@@ -203,11 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t idesc_qk = idesc_bf16(kM, kN, false, false);
   const uint32_t idesc_pv = idesc_bf16(kM, D, false, true);
-  const LogitXform xf{p.softmax_scale * p.k_scale, p.logits_soft_cap,
-                      p.logits_soft_cap > 0.f ? 1.f / p.logits_soft_cap : 0.f,
-                      p.softmax_scale * p.k_scale * kLog2e};
   const bool has_cap = p.logits_soft_cap > 0.f;
-  const float sc = has_cap ? 1.f : xf.scale_log2;  // raw score -> log2-domain logit
+  // the logit transform of the scalar key scale (used unless per-head scales)
+  const LogitXform xf0 = make_xform(p.softmax_scale, p.k_scale, p.logits_soft_cap);
 
   // Every role runs this loop over the CTA's units with its own body, so
   // the code of each role stays within its register budget; all threads meet
@@ -315,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         g.tile(j, is_new, key0, valid);
         uint8_t* op = smem + (kv ? kOffV : kOffK) + (tc & 1) * kOperand;
         const uint8_t* stg = smem + staging(tc, kv);
-        const float scale = kv ? p.v_scale : p.k_scale;
+        const float scale = !PH ? (kv ? p.v_scale : p.k_scale)
+                                : (kv ? v_scale_of(p, g.h) : k_scale_of(p, g.h));
         const int rows = kv ? kN : valid;
         for (int idx = lane; idx < rows * (D / 8); idx += 32) {
           const int r = idx / (D / 8), c = idx % (D / 8);
@@ -518,6 +517,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool is_new;
         int key0, valid;
         g.tile(j, is_new, key0, valid);
+        // with per-head scales the logit transform is formed per tile from a
+        // plain load of this head's scale (reissued after every barrier wait)
+        // rather than held in registers across the tile loop
+        const LogitXform xf =
+            PH ? make_xform(p.softmax_scale, p.k_scale_heads ? p.k_scale_heads[g.h] : p.k_scale,
+                            p.logits_soft_cap)
+               : xf0;
+        const float sc = has_cap ? 1.f : xf.mul;  // raw score -> log2-domain logit
         uint32_t sr[128];
         tmem_ld128(tS, sr);
         const bool full = valid == kN && key0 + kN - 1 <= pos && (W == 0 || pos - key0 < W);
@@ -592,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && !mbar_wait(bar(kBarODone + x), ucount & 1, &s_abort)) ok = false;
       if (ok) {
         tc_fence_after();
-        const float inv = p.v_scale / l_run;
+        const float inv = (PH ? v_scale_of(p, g.h) : p.v_scale) / l_run;
         __nv_bfloat16* dst = a.out + ((int64_t)(g.q0 + g.t_begin + ti) * p.num_q_heads + hq) * D;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -628,12 +635,12 @@ bool prefill_uses_tc(const rpa_params_t& p) {
   return (p.head_dim == 64 || p.head_dim == 128) && p.page_size >= 8 && G >= 1 && G <= 16;
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool PH>
 static cudaError_t launch_prefill_tc_t(const AttnArgs& a, int max_units, int num_sms,
                                        cudaStream_t stream) {
   using C = tc::TcCfg<D, FP8>;
   static std::atomic<unsigned long long> attr_done{0};
-  auto kern = tc::prefill_tc_kernel<D, FP8>;
+  auto kern = tc::prefill_tc_kernel<D, FP8, PH>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, &attr_done);
   if (e != cudaSuccess) return e;
   const rpa_params_t& p = a.kv.p;
@@ -660,11 +667,16 @@ static cudaError_t launch_prefill_tc_t(const AttnArgs& a, int max_units, int num
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream) {
   const bool fp8 = a.kv.p.kv_dtype == RPA_KV_FP8_E4M3;
+  // per-head scales get their own instantiation, so the common cases keep
+  // their logit transform loop-invariant
+  const bool ph = a.kv.p.k_scale_heads != nullptr || a.kv.p.v_scale_heads != nullptr;
   if (a.kv.p.head_dim == 64)
-    return fp8 ? launch_prefill_tc_t<64, true>(a, max_units, num_sms, stream)
-               : launch_prefill_tc_t<64, false>(a, max_units, num_sms, stream);
-  return fp8 ? launch_prefill_tc_t<128, true>(a, max_units, num_sms, stream)
-             : launch_prefill_tc_t<128, false>(a, max_units, num_sms, stream);
+    return !fp8 ? launch_prefill_tc_t<64, false, false>(a, max_units, num_sms, stream)
+           : ph  ? launch_prefill_tc_t<64, true, true>(a, max_units, num_sms, stream)
+                 : launch_prefill_tc_t<64, true, false>(a, max_units, num_sms, stream);
+  return !fp8 ? launch_prefill_tc_t<128, false, false>(a, max_units, num_sms, stream)
+         : ph  ? launch_prefill_tc_t<128, true, true>(a, max_units, num_sms, stream)
+               : launch_prefill_tc_t<128, true, false>(a, max_units, num_sms, stream);
 }
 
 }  // namespace rpa

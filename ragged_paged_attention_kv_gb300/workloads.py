@@ -63,6 +63,10 @@ class Workload:
     block_tables: np.ndarray           # [max_num_seqs * pages_per_seq] int32
     distribution: np.ndarray           # [3] int32
     total_tokens: int                  # rows of queries/keys/values/out
+    # optional per-kv-head fp8 scales [num_kv_heads] (fp32 numbers); they
+    # replace k_scale / v_scale head by head
+    k_scale_heads: Optional[np.ndarray] = None
+    v_scale_heads: Optional[np.ndarray] = None
 
     # ------------------------------------------------------------- metadata
     @property
@@ -114,7 +118,9 @@ class Workload:
                     kv_fp8=self.kv_dtype == "fp8", sliding_window=self.sliding_window,
                     softmax_scale=self.softmax_scale,
                     logits_soft_cap=self.logits_soft_cap,
-                    k_scale=self.k_scale, v_scale=self.v_scale)
+                    k_scale=self.k_scale, v_scale=self.v_scale,
+                    **({} if self.k_scale_heads is None else {"k_scale_heads": self.k_scale_heads}),
+                    **({} if self.v_scale_heads is None else {"v_scale_heads": self.v_scale_heads}))
 
     # --------------------------------------------------------------- tensors
     def _gen(self, stream: int) -> torch.Generator:
@@ -227,7 +233,8 @@ def make_custom(name: str, seed: int, q_lens, kv_lens, *, num_q_heads, num_kv_he
                 head_dim, page_size, num_pages=None, pool_slack=0.1, pages_per_seq=None,
                 max_num_seqs=None, kv_dtype="bf16", softmax_scale=None,
                 sliding_window=0, logits_soft_cap=0.0, k_scale=1.0, v_scale=1.0,
-                has_sink=False, distribution=None, extra_tokens=0) -> Workload:
+                has_sink=False, distribution=None, extra_tokens=0, k_scale_heads=None,
+                v_scale_heads=None) -> Workload:
     """A workload from explicit per-sequence (q_len, kv_len) lists."""
     q_lens = np.asarray(q_lens, dtype=np.int32)
     kv_lens = np.asarray(kv_lens, dtype=np.int32)
@@ -257,7 +264,11 @@ def make_custom(name: str, seed: int, q_lens, kv_lens, *, num_q_heads, num_kv_he
                     v_scale=float(v_scale), has_sink=bool(has_sink), q_lens=q_lens,
                     kv_lens_valid=kv_lens, block_tables=bt,
                     distribution=np.asarray(distribution, dtype=np.int32),
-                    total_tokens=int(q_lens.sum()) + int(extra_tokens))
+                    total_tokens=int(q_lens.sum()) + int(extra_tokens),
+                    k_scale_heads=None if k_scale_heads is None
+                    else np.asarray(k_scale_heads, np.float32),
+                    v_scale_heads=None if v_scale_heads is None
+                    else np.asarray(v_scale_heads, np.float32))
 
 
 def _randint(g, lo, hi, n):

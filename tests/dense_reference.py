@@ -27,14 +27,28 @@ def fp8_roundtrip(x_bf16: torch.Tensor, scale: float) -> np.ndarray:
     return q.to(torch.float64).numpy() * float(np.float32(scale))
 
 
-def pool_values(w, pool: torch.Tensor, scale: float) -> np.ndarray:
+def head_scales(w, kind: str) -> np.ndarray:
+    """[Hkv] fp64 values of the fp32 key ("k") or value ("v") scales: the
+    per-head ones when the workload has them, else the scalar repeated."""
+    per_head = w.k_scale_heads if kind == "k" else w.v_scale_heads
+    scalar = w.k_scale if kind == "k" else w.v_scale
+    if per_head is None:
+        return np.full(w.num_kv_heads, float(np.float32(scalar)))
+    return np.asarray(per_head, np.float32).astype(np.float64)
+
+
+def pool_values(w, pool: torch.Tensor) -> np.ndarray:
     """The pool as fp64 numbers [num_pages*P, 2Hkv, D] (fp8 codes dequantised
-    with torch's float8_e4m3fn)."""
+    with torch's float8_e4m3fn, channel 2h by head h's key scale and 2h+1 by
+    its value scale)."""
+    shape = (w.num_pages * w.page_size, 2 * w.num_kv_heads, w.head_dim)
     if w.kv_dtype == "fp8":
-        vals = pool.view(torch.float8_e4m3fn).to(torch.float64).numpy() * float(np.float32(scale))
-    else:
-        vals = pool.to(torch.float64).numpy()
-    return vals.reshape(w.num_pages * w.page_size, 2 * w.num_kv_heads, w.head_dim)
+        vals = pool.view(torch.float8_e4m3fn).to(torch.float64).numpy().reshape(shape)
+        chan = np.empty(2 * w.num_kv_heads)
+        chan[0::2] = head_scales(w, "k")
+        chan[1::2] = head_scales(w, "v")
+        return vals * chan[None, :, None]
+    return pool.to(torch.float64).numpy().reshape(shape)
 
 
 def logical_kv(w, pool_before: torch.Tensor, keys, values, s: int):
@@ -46,16 +60,17 @@ def logical_kv(w, pool_before: torch.Tensor, keys, values, s: int):
     kv_len = int(w.kv_lens_valid[s])
     ctx = kv_len - q_len
     Hkv = w.num_kv_heads
-    kpool = pool_values(w, pool_before, w.k_scale)
-    vpool = pool_values(w, pool_before, w.v_scale)
+    vals = pool_values(w, pool_before)
     slots = flat_slots(w, s, np.arange(ctx))
     K = np.empty((kv_len, Hkv, w.head_dim))
     V = np.empty((kv_len, Hkv, w.head_dim))
-    K[:ctx] = kpool[slots][:, 0::2, :]
-    V[:ctx] = vpool[slots][:, 1::2, :]
+    K[:ctx] = vals[slots][:, 0::2, :]
+    V[:ctx] = vals[slots][:, 1::2, :]
     if w.kv_dtype == "fp8":
-        K[ctx:] = fp8_roundtrip(keys[q0:q1], w.k_scale)
-        V[ctx:] = fp8_roundtrip(values[q0:q1], w.v_scale)
+        ks, vs = head_scales(w, "k"), head_scales(w, "v")
+        for h in range(Hkv):
+            K[ctx:, h] = fp8_roundtrip(keys[q0:q1, h], ks[h])
+            V[ctx:, h] = fp8_roundtrip(values[q0:q1, h], vs[h])
     else:
         K[ctx:] = keys[q0:q1].to(torch.float64).numpy()
         V[ctx:] = values[q0:q1].to(torch.float64).numpy()
@@ -110,8 +125,10 @@ def expected_pool_after(w, pool_before: torch.Tensor, keys, values) -> torch.Ten
             continue
         k, v = keys[q0:q1], values[q0:q1]
         if w.kv_dtype == "fp8":
-            k = (k.float() / torch.tensor(np.float32(w.k_scale))).to(torch.float8_e4m3fn).view(torch.uint8)
-            v = (v.float() / torch.tensor(np.float32(w.v_scale))).to(torch.float8_e4m3fn).view(torch.uint8)
+            ks = torch.tensor(head_scales(w, "k").astype(np.float32))[None, :, None]
+            vs = torch.tensor(head_scales(w, "v").astype(np.float32))[None, :, None]
+            k = (k.float() / ks).to(torch.float8_e4m3fn).view(torch.uint8)
+            v = (v.float() / vs).to(torch.float8_e4m3fn).view(torch.uint8)
         flat[slots, 0::2, :] = k
         flat[slots, 1::2, :] = v
     return pool

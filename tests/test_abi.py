@@ -43,6 +43,16 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+class _Ptr:
+    """Stands in for a device tensor: only its address reaches the host checks."""
+
+    def __init__(self, addr):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
+
+
 def _params(**over):
     from ragged_paged_attention_kv_gb300 import make_params
     kw = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16, num_pages=80000,
@@ -70,6 +80,8 @@ def test_workspace_size_host_only(lib):
     (dict(logits_soft_cap=-1.0), 1),
     (dict(softmax_scale=0.0), 1),
     (dict(softmax_scale=-0.5), 1),
+    (dict(k_scale_heads=_Ptr(256)), 1),           # per-head scales need an fp8 cache
+    (dict(kv_fp8=True, v_scale_heads=_Ptr(258)), 1),  # misaligned per-head scales
 ])
 def test_invalid_params_are_refused(lib, over, code):
     n = ctypes.c_size_t(0)

@@ -38,15 +38,21 @@ def run_gpu(w, q, k, v, pool_before, sink=None, workspace=None, out=None):
     out_t = out if out is not None else torch.full((w.total_tokens, w.num_q_heads, w.head_dim),
                                                    7.0, dtype=torch.bfloat16, device=DEV)
     params = rpa.make_params(**{k_: v_ for k_, v_ in w.params().items()
-                                if k_ not in ("kv_fp8",)}, kv_fp8=w.kv_dtype == "fp8")
+                                if k_ not in ("kv_fp8", "k_scale_heads", "v_scale_heads")},
+                             kv_fp8=w.kv_dtype == "fp8")
     ws = workspace if workspace is not None else rpa.alloc_workspace(params, DEV)
+    fp8 = w.kv_dtype == "fp8"
+    # per-kv-head scales go to the library as float32 device tensors
+    ks = _dev(w.k_scale_heads, torch.float32) if w.k_scale_heads is not None else \
+        (w.k_scale if fp8 else None)
+    vs = _dev(w.v_scale_heads, torch.float32) if w.v_scale_heads is not None else \
+        (w.v_scale if fp8 else None)
     rpa.forward(_dev(q), _dev(k), _dev(v), pool, _dev(w.kv_lens), _dev(w.block_tables),
                 _dev(w.query_start_loc), _dev(w.distribution),
                 None if sink is None else _dev(sink),
                 softmax_scale=w.softmax_scale, sliding_window=w.sliding_window,
-                logits_soft_cap=w.logits_soft_cap,
-                k_scale=w.k_scale if w.kv_dtype == "fp8" else None,
-                v_scale=w.v_scale if w.kv_dtype == "fp8" else None, out=out_t, workspace=ws)
+                logits_soft_cap=w.logits_soft_cap, k_scale=ks, v_scale=vs, out=out_t,
+                workspace=ws)
     status = rpa.get_status(ws)
     torch.cuda.synchronize()
     return out_t.float().cpu().numpy().astype(np.float64), pool.cpu(), status
@@ -112,6 +118,22 @@ CASES = [
                                v_scale=0.1, head_dim=128)),
     ("padding_rows", lambda: _case("pad", 117, [1, 5], [9, 12], max_num_seqs=5, extra_tokens=6,
                                    pages_per_seq=4)),
+    # per-kv-head fp8 scales: decode splits, the tcgen05 prefill (head_dim 64
+    # and 128), the mma.sync prefill (pages of 4 rows), with every option
+    ("fp8_per_head", lambda: _case("fh", 118, [1, 1, 40, 9], [1400, 70, 300, 9],
+                                   kv_dtype="fp8", num_q_heads=16, num_kv_heads=4,
+                                   k_scale_heads=[0.02, 0.05, 0.11, 0.3],
+                                   v_scale_heads=[0.07, 0.015, 0.2, 0.05])),
+    ("fp8_per_head_d128_options", lambda: _case(
+        "fhd", 119, [1, 1, 130, 33], [800, 40, 400, 33], kv_dtype="fp8", num_q_heads=16,
+        num_kv_heads=2, head_dim=128, k_scale_heads=[0.04, 0.09], v_scale_heads=[0.12, 0.03],
+        logits_soft_cap=20.0, has_sink=True, sliding_window=200)),
+    ("fp8_per_head_p4", lambda: _case("fh4", 120, [1, 25], [90, 60], kv_dtype="fp8",
+                                      page_size=4, k_scale_heads=[0.06, 0.02],
+                                      v_scale_heads=[0.03, 0.08])),
+    ("fp8_per_head_k_only", lambda: _case("fhk", 121, [1, 12], [300, 50], kv_dtype="fp8",
+                                          k_scale=0.05, v_scale=0.05,
+                                          k_scale_heads=[0.03, 0.07])),
 ]
 
 
@@ -258,6 +280,17 @@ def test_bad_distribution_plans_nothing():
     assert np.all(out == 7.0) and torch.equal(pool, pool_after)
 
 
+def test_bad_per_head_scale_sets_status():
+    from ragged_paged_attention_kv_gb300 import _lib
+    w = _case("bs", 135, [1, 4], [40, 30], kv_dtype="fp8", k_scale_heads=[0.05, 0.05],
+              v_scale_heads=[0.05, 0.05])
+
+    def mutate(w):
+        w.v_scale_heads = np.array([0.05, -0.5], np.float32)
+    status, _, _, _ = _status_of(w, mutate)
+    assert status == _lib.RPA_STATUS_BAD_SCALE
+
+
 def test_host_errors_raise():
     w = _case("he", 134, [1], [10])
     q, k, v = w.make_qkv()
@@ -268,19 +301,23 @@ def test_host_errors_raise():
 
 
 # ------------------------------------------------------------- update_cache
-@pytest.mark.parametrize("fp8", [False, True])
-def test_update_cache_alone_matches_oracle(fp8):
+@pytest.mark.parametrize("kind", ["bf16", "fp8", "fp8_per_head"])
+def test_update_cache_alone_matches_oracle(kind):
+    fp8 = kind != "bf16"
+    heads = dict(k_scale_heads=[0.03, 0.08], v_scale_heads=[0.2, 0.011]) \
+        if kind == "fp8_per_head" else {}
     w = _case("uc", 141, [1, 1, 40, 3], [90, 1, 40, 300], kv_dtype="fp8" if fp8 else "bf16",
-              k_scale=0.05 if fp8 else 1.0, v_scale=0.2 if fp8 else 1.0)
+              k_scale=0.05 if fp8 else 1.0, v_scale=0.2 if fp8 else 1.0, **heads)
     q, k, v = w.make_qkv()
     pool = w.make_pool("cpu")
     p = oracle.make_params(**w.params())
     ref = oracle.update_cache(p, k, v, pool_bytes(pool), w.kv_lens, w.block_tables,
                               w.query_start_loc, w.num_seqs)
     gpool = pool.to(DEV)
+    ks = _dev(w.k_scale_heads, torch.float32) if heads else (w.k_scale if fp8 else None)
+    vs = _dev(w.v_scale_heads, torch.float32) if heads else (w.v_scale if fp8 else None)
     rpa.update_cache(_dev(k), _dev(v), gpool, _dev(w.kv_lens), _dev(w.block_tables),
-                     _dev(w.query_start_loc), _dev(w.distribution),
-                     k_scale=w.k_scale if fp8 else None, v_scale=w.v_scale if fp8 else None,
+                     _dev(w.query_start_loc), _dev(w.distribution), k_scale=ks, v_scale=vs,
                      num_q_heads=w.num_q_heads)
     torch.cuda.synchronize()
     assert np.array_equal(pool_bytes(gpool.cpu()), ref)

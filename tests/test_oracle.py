@@ -119,6 +119,10 @@ SMALL_CASES = [
                               v_scale=0.08, logits_soft_cap=30.0, has_sink=True, sliding_window=5,
                               num_q_heads=8, num_kv_heads=2, page_size=4)),
     ("page32", lambda: _small("f", 16, [3, 1], [70, 45], page_size=32, head_dim=32)),
+    ("fp8_per_head", lambda: _small("pf", 18, [1, 6, 3], [27, 14, 3], kv_dtype="fp8",
+                                    num_q_heads=6, num_kv_heads=3,
+                                    k_scale_heads=[0.02, 0.09, 0.3],
+                                    v_scale_heads=[0.15, 0.04, 0.011], has_sink=True)),
     ("q_len0", lambda: _small("g", 17, [0, 4, 0], [5, 4, 11])),
 ]
 
@@ -354,3 +358,26 @@ def test_oracle_rejects_bad_metadata():
     assert oracle.check_distribution(p, np.array([1, 2, 2], np.int32), w.query_start_loc) == 0
     assert oracle.check_distribution(p, np.array([2, 2, 2], np.int32), w.query_start_loc) != 0
     assert oracle.check_distribution(p, np.array([1, 0, 2], np.int32), w.query_start_loc) != 0
+
+
+def test_equal_per_head_scales_are_the_scalar_scales():
+    """Per-kv-head scales that all equal the scalar ones give the same cache
+    bytes and outputs; one head's scale changed moves only that head's
+    channels and outputs."""
+    kw = dict(kv_dtype="fp8", num_q_heads=8, num_kv_heads=4, k_scale=0.05, v_scale=0.07)
+    base = _small("ph", 19, [1, 5], [23, 9], **kw)
+    same = _small("ph", 19, [1, 5], [23, 9], k_scale_heads=[0.05] * 4, v_scale_heads=[0.07] * 4,
+                  **kw)
+    one = _small("ph", 19, [1, 5], [23, 9], k_scale_heads=[0.05, 0.05, 0.2, 0.05],
+                 v_scale_heads=[0.07, 0.07, 0.02, 0.07], **kw)
+    q, k, v, pool, sink = _inputs(base)
+    o0, c0 = run_oracle(base, q, k, v, pool, sink)
+    o1, c1 = run_oracle(same, q, k, v, pool, sink)
+    o2, c2 = run_oracle(one, q, k, v, pool, sink)
+    assert np.array_equal(c0, c1) and np.array_equal(o0, o1)
+    # head 2 (q-heads 4, 5; pool channels 4, 5) differs, every other head is unchanged
+    assert not np.array_equal(o0[:, 4:6], o2[:, 4:6])
+    assert np.array_equal(np.delete(o0, [4, 5], axis=1), np.delete(o2, [4, 5], axis=1))
+    shape = (base.num_pages * base.page_size, 2 * base.num_kv_heads, base.head_dim)
+    d = (c0 != c2).reshape(shape).any(axis=(0, 2))
+    assert d[4] and d[5] and not d[[0, 1, 2, 3, 6, 7]].any()
