@@ -36,6 +36,10 @@ constexpr int kRescaleLog2 = 8;               // lazy-rescale threshold (log2 un
 
 template <int D, bool FP8>
 struct Cfg {
+  // head_dim 64 fits two CTAs per SM (registers and shared memory), which
+  // doubles the units in flight when short units make the path
+  // latency-bound; the per-SM ring depth stays the same
+  static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
   static constexpr int kRowBytes = FP8 ? D : 128;        // bytes of one box row in smem
   static constexpr int kHalves = FP8 ? 1 : D / 64;       // boxes across head_dim
   // a stage holds, per 64-wide half of head_dim, 2*kBN rows: key j at row 2j,
@@ -46,7 +50,8 @@ struct Cfg {
   static constexpr int kConvBytes = FP8 ? kConsumerWarps * 2 * kKeysPerWarp * D * 2 : 0;
   static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * (D + 2) * 4;
   // as many stages as fit next to the other buffers (at most 12, 160 KB)
-  static constexpr int kBudget = 220 * 1024 - 2 * kQBytes - kConvBytes - kMergeBytes - 1024 - 256;
+  static constexpr int kBudget =
+      (kCtasPerSm == 2 ? 110 : 220) * 1024 - 2 * kQBytes - kConvBytes - kMergeBytes - 1024 - 256;
   static constexpr int kStages1 = (kBudget < 160 * 1024 ? kBudget : 160 * 1024) / kStageBytes;
   static constexpr int kStages = kStages1 > 12 ? 12 : (kStages1 < 2 ? 2 : kStages1);
   // layout: [stages][q slots 2][conv][merge][unit info 2][barriers]
@@ -77,7 +82,7 @@ __device__ __forceinline__ uint32_t kv_addr(uint32_t stage, int r, int kv, int c
 }
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
     decode_kernel(const __grid_constant__ DecodeMaps maps, AttnArgs a) {
   using C = Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
@@ -557,7 +562,7 @@ static cudaError_t launch_decode_t(const AttnArgs& a, int max_units, int num_sms
                      2 * (uint64_t)p.num_kv_heads, (uint64_t)p.num_pages * p.page_size,
                      FP8 ? (uint32_t)D : 64u, 2u, rows, !FP8))
     return cudaErrorInvalidValue;
-  int grid = num_sms;
+  int grid = num_sms * C::kCtasPerSm;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
   kern<<<grid, dec::kThreads, C::kBytes, stream>>>(maps, a);
