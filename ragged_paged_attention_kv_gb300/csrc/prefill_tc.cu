@@ -39,7 +39,8 @@
 namespace rpa {
 namespace tc {
 
-// warpgroup 0: warp 0 TMA (+ fp8 decoding), warp 1 MMA, warps 2-3 idle;
+// warpgroup 0: warp 0 TMA (+ fp8 decoding), warp 1 MMA, warps 2-3 fp8 decoding
+// (idle for bf16 caches);
 // warpgroups 1 and 2: softmax of query tiles A and B
 constexpr int kThreads = 384;
 constexpr int kM = 128;         // rows per query tile (two per unit)
@@ -147,6 +148,8 @@ template <int D, bool FP8, bool PH>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ TcMaps maps, AttnArgs a) {
   using C = TcCfg<D, FP8>;
+  // warps that decode fp8 operands: the TMA warp and warps 2, 3
+  constexpr int kDecWarps = FP8 ? 3 : 1;
   constexpr uint32_t kOperand = C::kOperand, kOffQ = C::kOffQ, kOffK = C::kOffK,
                      kOffV = C::kOffV, kOffBar = C::kOffBar;
   extern __shared__ uint8_t smem_raw[];
@@ -177,9 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarKFull + s), 1);
       mbar_init(bar(kBarKEmpty + s), 1);
       mbar_init(bar(kBarVFull + s), 1);
-      mbar_init(bar(kBarVReady + s), 1);
+      mbar_init(bar(kBarVReady + s), FP8 ? kDecWarps : 1);
       mbar_init(bar(kBarVEmpty + s), 1);
-      mbar_init(bar(kBarKReady + s), 1);
+      mbar_init(bar(kBarKReady + s), kDecWarps);
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarPReady + s), 4);
       mbar_init(bar(kBarODone + s), 1);
@@ -211,6 +214,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the code of each role stays within its register budget; all threads meet
   // at the same two barriers per unit.  tcount counts the key tiles and
   // ucount the units the CTA has processed so far (all roles agree).
+  // fp8 cache: the staging buffer of an operand of tile tc, and the decoding
+  // of a landed operand of tile j into its bf16 stage, shared by kDecWarps
+  // warps (part 0..kDecWarps-1).  Cached rows are decoded from their e4m3
+  // codes; new rows, which came as bf16 from the inputs, are quantised and
+  // decoded in place so they carry exactly the codes the page write stores.
+  // Value rows past the valid range become zero; key rows there are masked
+  // by the softmax.
+  auto staging = [&](uint32_t tc, int kv) -> uint32_t {
+    return C::kOffStg + (2 * (C::kStgPerOp == 2 ? (tc & 1) : 0) + kv) * C::kStaging;
+  };
+  auto decode_fp8 = [&](const UnitGeom& g, uint32_t tc, int j, int kv, int part) {
+    bool is_new;
+    int key0, valid;
+    g.tile(j, is_new, key0, valid);
+    uint8_t* op = smem + (kv ? kOffV : kOffK) + (tc & 1) * kOperand;
+    const uint8_t* stg = smem + staging(tc, kv);
+    const float scale = !PH ? (kv ? p.v_scale : p.k_scale)
+                            : (kv ? v_scale_of(p, g.h) : k_scale_of(p, g.h));
+    const int rows = kv ? kN : valid;
+    for (int idx = 32 * part + lane; idx < rows * (D / 8); idx += 32 * kDecWarps) {
+      const int r = idx / (D / 8), c = idx % (D / 8);
+      uint4* dst = reinterpret_cast<uint4*>(op + (c >> 3) * kHalf + sw128(r, c & 7));
+      if (r >= valid) {
+        *dst = make_uint4(0, 0, 0, 0);
+      } else if (is_new) {
+        *dst = dequant8(quantize8(*dst, scale));
+      } else {
+        *dst = dequant8(*reinterpret_cast<const uint2*>(stg + r * D + c * 8));
+      }
+    }
+  };
+
   auto unit_loop = [&](auto&& body) {
     uint32_t tcount = 0, ucount = 0;
     for (;;) {
@@ -257,10 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pg0 = key0 / P, npg = (key0 + valid - 1) / P - pg0 + 1;
         return lane < npg ? __ldg(a.kv.block_tables + bt_row + pg0 + lane) : 0;
       };
-      // staging buffer of an fp8 operand of tile tc
-      auto staging = [&](uint32_t tc, int kv) -> uint32_t {
-        return C::kOffStg + (2 * (C::kStgPerOp == 2 ? (tc & 1) : 0) + kv) * C::kStaging;
-      };
       // issue the boxes of one operand (kv = 0 keys, 1 values) of tile j; each
       // lane copies its own page.  New tokens come as bf16 straight into the
       // operand stage; cached pages too for a bf16 cache, or as e4m3 codes
@@ -302,36 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      // fp8 cache: decode a landed operand of tile j into its bf16 stage.
-      // Cached rows are decoded from their e4m3 codes; new rows, which came
-      // as bf16 from the inputs, are quantised and decoded in place so they
-      // carry exactly the codes the page write stores.  Value rows past the
-      // valid range become zero; key rows there are masked by the softmax.
-      auto decode_fp8 = [&](uint32_t tc, int j, int kv) {
-        bool is_new;
-        int key0, valid;
-        g.tile(j, is_new, key0, valid);
-        uint8_t* op = smem + (kv ? kOffV : kOffK) + (tc & 1) * kOperand;
-        const uint8_t* stg = smem + staging(tc, kv);
-        const float scale = !PH ? (kv ? p.v_scale : p.k_scale)
-                                : (kv ? v_scale_of(p, g.h) : k_scale_of(p, g.h));
-        const int rows = kv ? kN : valid;
-        for (int idx = lane; idx < rows * (D / 8); idx += 32) {
-          const int r = idx / (D / 8), c = idx % (D / 8);
-          uint4* dst = reinterpret_cast<uint4*>(op + (c >> 3) * kHalf + sw128(r, c & 7));
-          if (r >= valid) {
-            *dst = make_uint4(0, 0, 0, 0);
-          } else if (is_new) {
-            *dst = dequant8(quantize8(*dst, scale));
-          } else {
-            *dst = dequant8(*reinterpret_cast<const uint2*>(stg + r * D + c * 8));
-          }
-        }
-      };
       auto finalize_k = [&](uint32_t tc, int j) -> bool {
         const int s = tc & 1;
         if (!mbar_wait(bar(kBarKFull + s), (tc >> 1) & 1, &s_abort)) return false;
-        decode_fp8(tc, j, 0);
+        decode_fp8(g, tc, j, 0, 0);
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarKReady + s));
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = tc & 1;
         if (!mbar_wait(bar(kBarVFull + s), (tc >> 1) & 1, &s_abort)) return false;
         if (FP8) {
-          decode_fp8(tc, j, 1);
+          decode_fp8(g, tc, j, 1, 0);
           fence_proxy_async();
         } else {
           bool is_new;
@@ -376,7 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ids = ids_next;
         if (j + 1 < nt) ids_next = load_ids(j + 1);
         if (kStg1 && j >= 1) {
-          ok = finalize_k(tc - 1, j - 1);
+          // the single staging buffer is refilled once every decoding warp
+          // is done with tile j-1's codes
+          ok = finalize_k(tc - 1, j - 1) &&
+               mbar_wait(bar(kBarKReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
           if (!ok) break;
         }
         if (!mbar_wait(bar(kBarKEmpty + s), par, &s_abort)) {
@@ -389,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         if (kStg1 && j >= 1) {
-          ok = finalize_v(tc - 1, j - 1);
+          ok = finalize_v(tc - 1, j - 1) &&
+               mbar_wait(bar(kBarVReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
           if (!ok) break;
         }
         if (!mbar_wait(bar(kBarVEmpty + s), par, &s_abort)) {
@@ -472,7 +481,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       });
     } else {
-      unit_loop([](const UnitGeom&, uint32_t, uint32_t) {});
+      if (FP8) {
+        // warps 2 and 3: their shares of the fp8 decoding, tile by tile
+        const int part = warp - 1;
+        unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t) {
+          bool ok = true;
+          for (int j = 0; j < g.n_tiles && ok; ++j) {
+            const uint32_t tc = tcount + j;
+            const int s = tc & 1;
+            for (int kv = 0; kv < 2 && ok; ++kv) {
+              ok = mbar_wait(bar((kv ? kBarVFull : kBarKFull) + s), (tc >> 1) & 1, &s_abort);
+              if (!ok) break;
+              decode_fp8(g, tc, j, kv, part);
+              fence_proxy_async();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar((kv ? kBarVReady : kBarKReady) + s));
+            }
+          }
+          if (!ok && lane == 0) {
+            set_status(hdr, RPA_STATUS_TIMEOUT);
+            s_abort = 1;
+          }
+        });
+      } else {
+        unit_loop([](const UnitGeom&, uint32_t, uint32_t) {});
+      }
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));

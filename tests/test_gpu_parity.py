@@ -291,6 +291,16 @@ def test_bad_per_head_scale_sets_status():
     assert status == _lib.RPA_STATUS_BAD_SCALE
 
 
+def test_empty_batch_is_a_no_op():
+    """distribution = [0, 0, 0]: no sequence, nothing planned, nothing written."""
+    w = _case("eb", 136, [1, 4], [40, 30], distribution=[0, 0, 0])
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu")
+    out, pool_after, status = run_gpu(w, q, k, v, pool)
+    assert status == 0
+    assert np.all(out == 7.0) and torch.equal(pool, pool_after)
+
+
 def test_host_errors_raise():
     w = _case("he", 134, [1], [10])
     q, k, v = w.make_qkv()
