@@ -16,6 +16,8 @@
 namespace rpa {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kSizeClasses = 16;  // decode sequences are ordered by these, longest first
+static_assert((kSizeClasses + 1) * 32 <= kPlanThreads, "one scan covers the class counts");
 
 // Block-wide exclusive scan of two ints per thread (one set of barriers for
 // both); returns the prefixes and writes the block totals to *total.  All
@@ -113,7 +115,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   __shared__ int2 s_scan[33];
   __shared__ unsigned long long s_keys;
   __shared__ int s_doff[kPlanThreads], s_poff[kPlanThreads], s_nsplit[kPlanThreads],
-      s_ntiles[kPlanThreads], s_lo[kPlanThreads], s_len[kPlanThreads], s_q0[kPlanThreads];
+      s_ntiles[kPlanThreads], s_lo[kPlanThreads], s_len[kPlanThreads], s_q0[kPlanThreads],
+      s_seq[kPlanThreads], s_wbase[kPlanThreads];
+  __shared__ int s_maxkey;
   const WorkspaceLayout L(p);
   DecodeUnit* dunits = reinterpret_cast<DecodeUnit*>(reinterpret_cast<char*>(ws) + L.decode_units_off);
   PrefillUnit* punits =
@@ -130,6 +134,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   if (tid == 0) {
     s_flags = 0;
     s_keys = 0ull;
+    s_maxkey = 0;
   }
   __syncthreads();
   const int d0 = dist[0], d1 = dist[1], d2 = dist[2];
@@ -151,11 +156,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
 
   // Pass 1: total decode keys (per kv head) to size the splits.
   unsigned long long my_keys = 0;
+  int my_max = 0;
   for (int s = tid; s < S; s += kPlanThreads) {
     SeqPlan sp = classify(p, s, d0, s == tid ? meta0 : load_meta(s, kv_lens, qsl));
     if (sp.flags) atomicOr(&s_flags, sp.flags);
-    if (sp.cls == 1) my_keys += (unsigned long long)(sp.kv_len - sp.lo);
+    if (sp.cls == 1) {
+      my_keys += (unsigned long long)(sp.kv_len - sp.lo);
+      my_max = max(my_max, sp.kv_len - sp.lo);
+    }
   }
+  my_max = __reduce_max_sync(0xffffffffu, my_max);
+  if ((tid & 31) == 0 && my_max) atomicMax(&s_maxkey, my_max);
   // warp sums first: one shared atomic per warp, not per thread
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) my_keys += __shfl_xor_sync(0xffffffffu, my_keys, o);
@@ -183,20 +194,47 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
       if (sp.cls == 1) nsplit = (sp.kv_len - (sp.lo & ~63) + chunk - 1) / chunk;
       if (sp.cls == 2) ntiles = (sp.q_len + tile_tokens - 1) / tile_tokens;
     }
-    int2 totals;
-    const int2 offs = block_exclusive_scan2(make_int2(nsplit * Hkv, ntiles * Hkv), &totals, s_scan);
-    const int dec_off = offs.x, pf_off = offs.y, dec_total = totals.x, pf_total = totals.y;
-    s_doff[tid] = dec_off;
-    s_poff[tid] = pf_off;
     s_nsplit[tid] = nsplit;
     s_ntiles[tid] = ntiles;
     s_lo[tid] = sp.lo;
     s_len[tid] = sp.cls == 1 ? sp.kv_len : sp.q_len;
     s_q0[tid] = sp.q0;
+    // Decode sequences are ranked longest first (16 size classes of the
+    // keys they read, the sequence index inside a class; the other
+    // sequences last), so the dynamic scheduler hands out the longest decode
+    // units first and the kernel's tail is made of short ones.  Counting
+    // sort: rank = base of (class, warp) + rank among the warp's lanes of
+    // the same class.
+    {
+      const int kb = sp.cls == 1 ? (int)((int64_t)(s_maxkey - (sp.kv_len - sp.lo)) * kSizeClasses /
+                                         ((int64_t)s_maxkey + 1))
+                                 : kSizeClasses;
+      const unsigned same = __match_any_sync(0xffffffffu, kb);
+      const int lane = tid & 31, warp = tid >> 5;
+      s_wbase[tid] = 0;
+      __syncthreads();
+      if (lane == __ffs(same) - 1) s_wbase[kb * 32 + warp] = __popc(same);
+      __syncthreads();
+      // (class, warp) counts in class-major order -> exclusive bases
+      int2 cb_total;
+      const int2 cb = block_exclusive_scan2(make_int2(s_wbase[tid], 0), &cb_total, s_scan);
+      __syncthreads();
+      s_wbase[tid] = cb.x;
+      __syncthreads();
+      s_seq[s_wbase[kb * 32 + warp] + __popc(same & ((1u << lane) - 1u))] = tid;
+    }
+    __syncthreads();
+    const int si = s_seq[tid];  // sequence at rank tid
+    int2 totals;
+    const int2 offs = block_exclusive_scan2(make_int2(s_nsplit[si] * Hkv, ntiles * Hkv), &totals, s_scan);
+    const int dec_off = offs.x, pf_off = offs.y, dec_total = totals.x, pf_total = totals.y;
+    s_doff[tid] = dec_off;  // by rank
+    s_poff[tid] = pf_off;   // by sequence
     __syncthreads();
     for (int u = tid; u < dec_total; u += kPlanThreads) {
-      const int i = last_at_or_below(s_doff, kPlanThreads, u);
-      const int ns = s_nsplit[i], r = u - s_doff[i];
+      const int ri = last_at_or_below(s_doff, kPlanThreads, u);
+      const int i = s_seq[ri];
+      const int ns = s_nsplit[i], r = u - s_doff[ri];
       const int h = r / ns, k = r % ns;
       const int lo = s_lo[i], kv = s_len[i];
       const int stage0 = lo & ~63;  // split boundaries on 64-key stages
