@@ -38,10 +38,14 @@ struct PrefillUnit {
   int32_t seq, t_begin, t_end, head;    // new tokens [t_begin, t_end) of seq
 };
 
+// The planner splits a decode sequence's keys only when the batch has too
+// few (sequence, kv head) pairs to keep the GPU busy: splits aim at about
+// this many units in total.  Units are handed out longest first, so the
+// pairs need no splitting to balance.
 #ifndef RPA_DECODE_UNITS_TARGET
-#define RPA_DECODE_UNITS_TARGET 1024
+#define RPA_DECODE_UNITS_TARGET 512
 #endif
-constexpr int kDecodeUnitsTarget = RPA_DECODE_UNITS_TARGET;  // planner aims for about this many splits
+constexpr int kDecodeUnitsTarget = RPA_DECODE_UNITS_TARGET;
 constexpr int kDecodeChunkMin = 256;      // smallest split, in keys
 constexpr int kDecodeRows = 16;           // q-heads per decode tile (padded group)
 constexpr int kPrefillRows = 64;          // packed (token, q-head) rows per prefill tile
