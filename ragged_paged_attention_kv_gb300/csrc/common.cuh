@@ -59,7 +59,12 @@ struct WorkspaceLayout {
 
   __host__ __device__ explicit WorkspaceLayout(const rpa_params_t& p) {
     const int64_t g = p.num_q_heads / p.num_kv_heads;
-    max_decode_units = (int64_t)kDecodeUnitsTarget + (int64_t)p.max_num_seqs * p.num_kv_heads;
+    // A decode sequence with K keys spans at most K + 63 keys from the 64-key
+    // stage below its first key, so it takes ceil((K + 63) / chunk) <= K /
+    // chunk + 63 / chunk + 1 splits per kv head; with chunk >= total keys *
+    // Hkv / target and chunk >= 256 the units number at most target +
+    // (1 + 63/256) * sequences * Hkv.
+    max_decode_units = (int64_t)kDecodeUnitsTarget + 2 * (int64_t)p.max_num_seqs * p.num_kv_heads;
     const int64_t tiles = ((int64_t)p.total_tokens * g + kPrefillRows - 1) / kPrefillRows +
                           p.max_num_seqs;
     max_prefill_units = tiles * p.num_kv_heads;

@@ -291,6 +291,17 @@ def test_bad_per_head_scale_sets_status():
     assert status == _lib.RPA_STATUS_BAD_SCALE
 
 
+def test_decode_units_fill_the_workspace_bound():
+    """65 decode sequences x 8 kv heads, window 1000 starting 63 keys into a
+    64-key stage: with the split target of 512 the chunk is 1024 keys and
+    every (sequence, head) spans 1063 keys, so each takes two splits -- 1040
+    units, more than target + sequences * heads.  The workspace must hold them
+    and the results must match the oracle."""
+    S = 65
+    kv = [1063 + 64 * (s % 4) for s in range(S)]
+    check_case(_case("wb", 137, [1] * S, kv, num_q_heads=8, num_kv_heads=8, sliding_window=1000))
+
+
 def test_empty_batch_is_a_no_op():
     """distribution = [0, 0, 0]: no sequence, nothing planned, nothing written."""
     w = _case("eb", 136, [1, 4], [40, 30], distribution=[0, 0, 0])
