@@ -268,6 +268,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         const int col = (2 * ks + (mi >> 1)) * 16;
         ldmatrix_x4(sq + row * (D * 2) + col, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
       }
+      // The slot is refilled by a bulk copy (async proxy) once all warps
+      // have arrived, and nothing reads qa before the first stage lands, so
+      // the ldmatrix reads may still be in flight here: a proxy fence orders
+      // them before the release (without it, a short unit's later column
+      // blocks were seen to hold the next query routed to this slot).
+      fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_qempty + 8 * slot);
     }
