@@ -296,7 +296,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       const int kw = kb0 + st * kBN + warp * kKeysPerWarp;  // this warp's first key
       uint32_t tK, tV;
       int krow0;
-      bool wrote = false;
       if (FP8) {
         // convert this warp's 16 keys/values to bf16 in its own buffer; keys
         // outside the unit become zero, the new token comes from the inputs
@@ -351,7 +350,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
                   __ldg(reinterpret_cast<const uint4*>(a.kv.values + off));
             }
           }
-          wrote = true;
           __syncwarp();
         }
       }
@@ -432,7 +430,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         mma_bf16_16816(o[2 * cp], pa, b0, b1);
         mma_bf16_16816(o[2 * cp + 1], pa, b2, b3);
       }
-      if (wrote) fence_proxy_async();  // our stores precede the next TMA into this stage
+      // this warp's reads of the stage (and its edge stores) precede the
+      // next TMA into it: the generic-to-async proxy fence orders them
+      fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
