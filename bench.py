@@ -57,6 +57,10 @@ DESCRIPTIONS = {
     "fp8_small": "fp8 shape at profiling size: 64 decode + 8x256 chunks; e4m3 cache, cap 30, "
                  "sinks, window 128; Hq64/Hkv8/D64, page_size 16",
     "tiny": "tiny mixed batch: 3 seqs (1,17),(24,24),(5,40); Hq4/Hkv2/D64/P16",
+    "decode_d256": "decode, Gemma-2-9B attention shape (head_dim 256): 256 seqs q_len=1, "
+                   "kv_len~U[512,4096]; Hq16/Hkv8/D256, window 4096, soft cap 50, scale 1/16, "
+                   "bf16 cache, page_size 16, pool = pages used + 10%",
+    "decode_d256_small": "decode_d256 shape at 64 seqs (profiling size)",
 }
 
 

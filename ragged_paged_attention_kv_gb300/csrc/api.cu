@@ -22,7 +22,7 @@ static int check_params(const rpa_params_t* p) {
   if (p->num_q_heads % p->num_kv_heads != 0) return RPA_ERR_UNSUPPORTED;
   const int G = p->num_q_heads / p->num_kv_heads;
   if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16)) return RPA_ERR_UNSUPPORTED;
-  if (p->head_dim != 64 && p->head_dim != 128) return RPA_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return RPA_ERR_UNSUPPORTED;
   if (!is_pow2(p->page_size) || p->page_size > 1024) return RPA_ERR_UNSUPPORTED;
   if (p->kv_dtype != RPA_KV_BF16 && p->kv_dtype != RPA_KV_FP8_E4M3) return RPA_ERR_UNSUPPORTED;
   // fp8 rows of 64 bytes need at least two rows per page for 128-byte aligned copies

@@ -46,7 +46,13 @@ struct Cfg {
   // value j at row 2j+1 (one TMA box brings both for a page)
   static constexpr int kHalfBytes = 2 * kBN * kRowBytes;
   static constexpr int kStageBytes = kHalves * kHalfBytes;
-  static constexpr int kQBytes = kDecodeRows * D * 2;    // one query slot
+  // head_dim 256: the query fragments (64 registers) are re-read from the
+  // slot every stage instead of being held, and each row lands with its own
+  // bulk copy at a 16-byte padded stride, so those ldmatrix reads are free
+  // of bank conflicts; the slot is then released at the end of the unit
+  static constexpr bool kQFromSmem = D > 128;
+  static constexpr int kQRow = kQFromSmem ? D * 2 + 16 : D * 2;  // bytes per query row
+  static constexpr int kQBytes = kDecodeRows * kQRow;    // one query slot
   static constexpr int kConvBytes = FP8 ? kConsumerWarps * 2 * kKeysPerWarp * D * 2 : 0;
   static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * (D + 2) * 4;
   // as many stages as fit next to the other buffers (at most 12, 160 KB)
@@ -61,6 +67,7 @@ struct Cfg {
   static constexpr int kOffInfo = kOffMerge + kMergeBytes;
   static constexpr int kOffBar = kOffInfo + 2 * 64;  // two UnitInfo slots
   static constexpr int kBytes = kOffBar + (2 * kStages + 4) * 8 + 1024;  // + base alignment
+  static_assert(kBytes <= 227 * 1024 / kCtasPerSm, "decode shared memory over budget");
 };
 
 // What the producer tells the consumers about the unit in a query slot.
@@ -111,9 +118,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
   const int P = p.page_size;
   if (hdr[kHdrNumDecode] == 0) return;  // a prefill-only batch: nothing to set up
 
-  // zero both query slots (rows >= G stay zero), init barriers
+  // zero both query slots (rows >= G stay zero), init barriers; the bulk
+  // copies that later fill rows < G are async-proxy writes of the same bytes
   for (int i = tid; i < 2 * C::kQBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(smem + C::kOffQ)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async();
   if (tid == 0) {
     s_abort = 0;
     for (int s = 0; s < C::kStages; ++s) {
@@ -190,9 +199,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         info[slot] = ui;
         const uint32_t qbytes = (uint32_t)(G * D * 2);
         mbar_arrive_expect_tx(bar_qfull + 8 * slot, qbytes);
-        bulk_load(s_base + C::kOffQ + slot * C::kQBytes,
-                  a.queries + ((int64_t)q0 * p.num_q_heads + du.head * G) * D, qbytes,
-                  bar_qfull + 8 * slot);
+        if (!C::kQFromSmem)
+          bulk_load(s_base + C::kOffQ + slot * C::kQBytes,
+                    a.queries + ((int64_t)q0 * p.num_q_heads + du.head * G) * D, qbytes,
+                    bar_qfull + 8 * slot);
+      }
+      if (C::kQFromSmem) {  // one row per lane at the padded stride
+        __syncwarp();       // the expected bytes are posted first
+        if (lane < G)
+          bulk_load(s_base + C::kOffQ + slot * C::kQBytes + lane * C::kQRow,
+                    a.queries + ((int64_t)q0 * p.num_q_heads + du.head * G + lane) * D,
+                    (uint32_t)(D * 2), bar_qfull + 8 * slot);
       }
       for (int st = 0; st < n_st; ++st, ++g) {
         int ids[2] = {ids_next[0], ids_next[1]};
@@ -255,19 +272,21 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
     // split 0 stores the new token's key/value into its page after the
     // stages; the page id and the inputs are loaded now so that store does
     // not wait for them
-    TokenKvLane tkv{};
-    if (du.split == 0 && warp == 0) tkv = token_kv_load<FP8>(a.kv, seq, q0, ctx, h, lane);
+    TokenKv<D> tkv{};
+    if (du.split == 0 && warp == 0) tkv = token_kv_load<FP8, D>(a.kv, seq, q0, ctx, h, lane);
 
-    uint32_t qa[D / 16][4];
-    {
-      const uint32_t sq = s_base + C::kOffQ + slot * C::kQBytes;
+    // query fragment ks of this warp's 16-row tile
+    const uint32_t sq = s_base + C::kOffQ + slot * C::kQBytes;
+    auto load_q = [&](int ks, uint32_t (&f)[4]) {
+      const int mi = lane >> 3;
+      const int row = (lane & 7) + ((mi & 1) << 3);
+      const int col = (2 * ks + (mi >> 1)) * 16;
+      ldmatrix_x4(sq + row * C::kQRow + col, f[0], f[1], f[2], f[3]);
+    };
+    uint32_t qa[C::kQFromSmem ? 1 : D / 16][4];
+    if constexpr (!C::kQFromSmem) {
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int mi = lane >> 3;
-        const int row = (lane & 7) + ((mi & 1) << 3);
-        const int col = (2 * ks + (mi >> 1)) * 16;
-        ldmatrix_x4(sq + row * (D * 2) + col, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-      }
+      for (int ks = 0; ks < (C::kQFromSmem ? 1 : D / 16); ++ks) load_q(ks, qa[ks]);
       // The slot is refilled by a bulk copy (async proxy) once all warps
       // have arrived, and nothing reads qa before the first stage lands, so
       // the ldmatrix reads may still be in flight here: a proxy fence orders
@@ -366,8 +385,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         const uint32_t addr = FP8 ? tK + swz(key, chunk, D * 2) : kv_addr(tK, key, 0, chunk);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(addr, b0, b1, b2, b3);
-        mma_bf16_16816(sc[0], qa[ks], b0, b1);
-        mma_bf16_16816(sc[1], qa[ks], b2, b3);
+        if constexpr (C::kQFromSmem) {
+          uint32_t qf[4];
+          load_q(ks, qf);
+          mma_bf16_16816(sc[0], qf, b0, b1);
+          mma_bf16_16816(sc[1], qf, b2, b3);
+        } else {
+          mma_bf16_16816(sc[0], qa[C::kQFromSmem ? 0 : ks], b0, b1);
+          mma_bf16_16816(sc[1], qa[C::kQFromSmem ? 0 : ks], b2, b3);
+        }
       }
       // logits, mask, online softmax (rows gq and gq + 8)
       float mx[2] = {-INFINITY, -INFINITY};
@@ -436,13 +462,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
+    if constexpr (C::kQFromSmem) {  // the query slot was read up to the last stage
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_qempty + 8 * slot);
+    }
     if (!ok) {
       set_status(hdr, RPA_STATUS_TIMEOUT);
       s_abort = 1;
       break;
     }
 
-    if (du.split == 0 && warp == 0) token_kv_store<FP8>(a.kv, tkv, ctx, h, lane);
+    if (du.split == 0 && warp == 0) token_kv_store<FP8, D>(a.kv, tkv, ctx, h, lane);
 
     // per-warp state -> shared memory rows [warp][row] of (m, l, O[D]); only
     // the G rows of the GQA group are real, the rest of the 16-row tile is
@@ -580,6 +611,9 @@ cudaError_t launch_decode(const AttnArgs& a, int max_units, int num_sms, cudaStr
   if (a.kv.p.head_dim == 64)
     return fp8 ? launch_decode_t<64, true>(a, max_units, num_sms, stream)
                : launch_decode_t<64, false>(a, max_units, num_sms, stream);
+  if (a.kv.p.head_dim == 256)
+    return fp8 ? launch_decode_t<256, true>(a, max_units, num_sms, stream)
+               : launch_decode_t<256, false>(a, max_units, num_sms, stream);
   return fp8 ? launch_decode_t<128, true>(a, max_units, num_sms, stream)
              : launch_decode_t<128, false>(a, max_units, num_sms, stream);
 }

@@ -69,42 +69,56 @@ __device__ __forceinline__ void write_token_kv(const KvArgs& a, int seq, int t, 
 
 // The same write for one token split into its two halves, so that a caller
 // can issue the page-id and input loads early and store later: lane l holds
-// 16-byte chunk l of the token's key row then value row (head_dim <= 128).
-// Nothing reads the loaded values before token_kv_store, so the loads do
-// not stall the caller in between.
-struct TokenKvLane {
-  int32_t page;  // block-table entry of the token's slot
-  uint4 x;       // the chunk's bf16 input
+// 16-byte chunks l, l + 32, ... of the token's key row followed by its value
+// row (one chunk per lane up to head_dim 128, two at 256).  Nothing reads
+// the loaded values before token_kv_store, so the loads do not stall the
+// caller in between.
+template <int D>
+struct TokenKv {
+  static constexpr int kChunks = D / 8;                   // 16-byte chunks of one row
+  static constexpr int kPerLane = (2 * kChunks + 31) / 32;  // chunks held by each lane
+  int32_t page;        // block-table entry of the token's slot
+  uint4 x[kPerLane];   // the chunks' bf16 inputs
 };
-template <bool FP8>
-__device__ __forceinline__ TokenKvLane token_kv_load(const KvArgs& a, int seq, int t, int pos,
-                                                     int h, int lane) {
-  TokenKvLane r{0, make_uint4(0, 0, 0, 0)};
-  const int D = a.p.head_dim;
-  const int chunks = D / 8;
-  if (lane >= 2 * chunks) return r;
-  const int kv = lane / chunks, c = lane % chunks;
+template <bool FP8, int D>
+__device__ __forceinline__ TokenKv<D> token_kv_load(const KvArgs& a, int seq, int t, int pos,
+                                                    int h, int lane) {
+  using T = TokenKv<D>;
+  T r;
   r.page = __ldg(a.block_tables + (int64_t)seq * a.p.pages_per_seq + pos / a.p.page_size);
-  r.x = __ldg(reinterpret_cast<const uint4*>((kv ? a.values : a.keys) +
-                                             ((int64_t)t * a.p.num_kv_heads + h) * D + c * 8));
+#pragma unroll
+  for (int j = 0; j < T::kPerLane; ++j) {
+    const int i = lane + 32 * j;
+    r.x[j] = make_uint4(0, 0, 0, 0);
+    if (i < 2 * T::kChunks) {
+      const int kv = i / T::kChunks, c = i % T::kChunks;
+      r.x[j] = __ldg(reinterpret_cast<const uint4*>(
+          (kv ? a.values : a.keys) + ((int64_t)t * a.p.num_kv_heads + h) * D + c * 8));
+    }
+  }
   return r;
 }
-template <bool FP8>
-__device__ __forceinline__ void token_kv_store(const KvArgs& a, const TokenKvLane& r, int pos,
+template <bool FP8, int D>
+__device__ __forceinline__ void token_kv_store(const KvArgs& a, const TokenKv<D>& r, int pos,
                                                int h, int lane) {
-  const int chunks = a.p.head_dim / 8;
-  if (lane >= 2 * chunks) return;
+  using T = TokenKv<D>;
+  if (lane >= 2 * T::kChunks) return;
   if (r.page < 0 || r.page >= a.p.num_pages) {
     set_status(a.ws, RPA_STATUS_BAD_PAGE);
     return;
   }
-  const int kv = lane / chunks, c = lane % chunks;
-  const int64_t dst = pool_offset(a.p, r.page, pos % a.p.page_size, 2 * h + kv, FP8 ? 1 : 2);
-  if (FP8)
-    *reinterpret_cast<uint2*>(a.cache + dst + c * 8) =
-        quantize8(r.x, kv ? v_scale_of(a.p, h) : k_scale_of(a.p, h));
-  else
-    *reinterpret_cast<uint4*>(a.cache + dst + c * 16) = r.x;
+#pragma unroll
+  for (int j = 0; j < T::kPerLane; ++j) {
+    const int i = lane + 32 * j;
+    if (i >= 2 * T::kChunks) continue;
+    const int kv = i / T::kChunks, c = i % T::kChunks;
+    const int64_t dst = pool_offset(a.p, r.page, pos % a.p.page_size, 2 * h + kv, FP8 ? 1 : 2);
+    if (FP8)
+      *reinterpret_cast<uint2*>(a.cache + dst + c * 8) =
+          quantize8(r.x[j], kv ? v_scale_of(a.p, h) : k_scale_of(a.p, h));
+    else
+      *reinterpret_cast<uint4*>(a.cache + dst + c * 16) = r.x[j];
+  }
 }
 
 // One warp writes key and value head `h` of the n consecutive input tokens

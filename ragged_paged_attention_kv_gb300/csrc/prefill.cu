@@ -147,7 +147,17 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    uint32_t qa[D / 16][4];
+    // query fragment ks of this warp's 16 rows; up to head_dim 128 they are
+    // held in registers for the whole unit, at 256 (64 registers) they are
+    // re-read from the swizzled Q tile for every key tile
+    constexpr bool kQFromSmem = D > 128;
+    auto load_q = [&](int ks, uint32_t (&f)[4]) {
+      const int mi = lane >> 3;
+      const int row = warp * 16 + (lane & 7) + ((mi & 1) << 3);
+      const int chunk = 2 * ks + (mi >> 1);
+      ldmatrix_x4(smem_u32(sQ + swz(row, chunk, D * 2)), f[0], f[1], f[2], f[3]);
+    };
+    uint32_t qa[kQFromSmem ? 1 : D / 16][4];
 
     for (int kt = 0; kt < n_kt; ++kt) {
       if (kt + 1 < n_kt)
@@ -156,14 +166,10 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
       cp_async_commit();
       cp_async_wait<1>();
       __syncthreads();
-      if (kt == 0) {
+      if constexpr (!kQFromSmem) {
+        if (kt == 0) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int mi = lane >> 3;
-          const int row = warp * 16 + (lane & 7) + ((mi & 1) << 3);
-          const int chunk = 2 * ks + (mi >> 1);
-          ldmatrix_x4(smem_u32(sQ + swz(row, chunk, D * 2)), qa[ks][0], qa[ks][1], qa[ks][2],
-                      qa[ks][3]);
+          for (int ks = 0; ks < (kQFromSmem ? 1 : D / 16); ++ks) load_q(ks, qa[ks]);
         }
       }
       const uint8_t* tK = sStages + (kt % kStages) * S::kStageBytes;
@@ -175,6 +181,13 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
       for (int n = 0; n < kBN / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t qf[4];
+        if constexpr (kQFromSmem) {
+          load_q(ks, qf);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) qf[i] = qa[kQFromSmem ? 0 : ks][i];
+        }
 #pragma unroll
         for (int np = 0; np < kBN / 16; ++np) {
           const int mi = lane >> 3;
@@ -182,8 +195,8 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
           const int chunk = 2 * ks + (mi & 1);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(smem_u32(tK + swz(key, chunk, D * 2)), b0, b1, b2, b3);
-          mma_bf16_16816(s[2 * np], qa[ks], b0, b1);
-          mma_bf16_16816(s[2 * np + 1], qa[ks], b2, b3);
+          mma_bf16_16816(s[2 * np], qf, b0, b1);
+          mma_bf16_16816(s[2 * np + 1], qf, b2, b3);
         }
       }
       // does any key of this tile need masking for this warp's rows?
@@ -314,6 +327,9 @@ cudaError_t launch_prefill(const AttnArgs& a, int max_units, int num_sms, cudaSt
   if (a.kv.p.head_dim == 64)
     return fp8 ? launch_prefill_t<64, true>(a, max_units, num_sms, stream)
                : launch_prefill_t<64, false>(a, max_units, num_sms, stream);
+  if (a.kv.p.head_dim == 256)
+    return fp8 ? launch_prefill_t<256, true>(a, max_units, num_sms, stream)
+               : launch_prefill_t<256, false>(a, max_units, num_sms, stream);
   return fp8 ? launch_prefill_t<128, true>(a, max_units, num_sms, stream)
              : launch_prefill_t<128, false>(a, max_units, num_sms, stream);
 }

@@ -313,6 +313,27 @@ def decode() -> Workload:
                     distribution=np.array([S, S, S], np.int32), total_tokens=S)
 
 
+def decode_d256(S: int = 256, name: str = "decode_d256") -> Workload:
+    """Decode with Gemma-2-9B's attention shape (head_dim 256): Hq16/Hkv8,
+    sliding window 4096, logit soft cap 50, softmax scale 1/16; S sequences of
+    one new token each with kv_len ~ U[512, 4096], bf16 cache, page_size 16."""
+    seed = 1009
+    g = torch.Generator().manual_seed(seed)
+    P = 16
+    kv = _randint(g, 512, 4096, S)
+    q = np.ones(S, np.int32)
+    pps = 4096 // P
+    need = int(sum(-(-int(k) // P) for k in kv))
+    num_pages = int(need * 1.1) + 1
+    bt = _assign_pages(kv, P, num_pages, S, pps, g)
+    return Workload(name=name, seed=seed, num_q_heads=16, num_kv_heads=8, head_dim=256,
+                    page_size=P, num_pages=num_pages, pages_per_seq=pps, max_num_seqs=S,
+                    kv_dtype="bf16", softmax_scale=1.0 / 16.0, sliding_window=4096,
+                    logits_soft_cap=50.0, k_scale=1.0, v_scale=1.0, has_sink=False,
+                    q_lens=q, kv_lens_valid=kv, block_tables=bt,
+                    distribution=np.array([S, S, S], np.int32), total_tokens=S)
+
+
 def decode_small() -> Workload:
     """The decode workload's shape and length mix at a quarter of the batch
     (64 sequences) with a pool of the pages used + 10%: small enough for a
@@ -443,6 +464,8 @@ WORKLOADS = {
     "long_small": long_small,
     "fp8": fp8,
     "fp8_small": fp8_small,
+    "decode_d256": decode_d256,
+    "decode_d256_small": lambda: decode_d256(64, "decode_d256_small"),
 }
 
 

@@ -68,8 +68,17 @@ def test_workspace_size_host_only(lib):
     assert workspace_size(_params(total_tokens=65536, max_num_seqs=2)) > 0
 
 
+@pytest.mark.parametrize("head_dim", [64, 128, 256])
+def test_supported_head_dims(lib, head_dim):
+    n = ctypes.c_size_t(0)
+    p = _params(head_dim=head_dim)
+    assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0 and n.value > 0
+
+
 @pytest.mark.parametrize("over,code", [
     (dict(head_dim=96), 2),
+    (dict(head_dim=192), 2),
+    (dict(head_dim=512), 2),
     (dict(num_q_heads=24, num_kv_heads=8), 2),
     (dict(num_q_heads=30, num_kv_heads=8), 2),
     (dict(page_size=24), 2),

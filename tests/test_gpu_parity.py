@@ -134,6 +134,26 @@ CASES = [
     ("fp8_per_head_k_only", lambda: _case("fhk", 121, [1, 12], [300, 50], kv_dtype="fp8",
                                           k_scale=0.05, v_scale=0.05,
                                           k_scale_heads=[0.03, 0.07])),
+    # head_dim 256: decode (query fragments re-read from a padded slot) and
+    # the warp-level MMA prefill
+    ("d256_decode_splits", lambda: _case("e1", 122, [1] * 6, [700, 17, 1, 16, 33, 1290],
+                                         num_q_heads=16, num_kv_heads=8, head_dim=256)),
+    ("d256_prefill", lambda: _case("e2", 123, [150, 37, 1, 64], [150, 300, 90, 64],
+                                   num_q_heads=8, num_kv_heads=4, head_dim=256)),
+    ("d256_gemma_options", lambda: _case("e3", 124, [1, 1, 40, 9], [300, 5, 140, 9],
+                                         num_q_heads=16, num_kv_heads=8, head_dim=256,
+                                         sliding_window=64, logits_soft_cap=50.0,
+                                         has_sink=True, softmax_scale=0.0625,
+                                         distribution=[2, 3, 4])),
+    ("d256_fp8", lambda: _case("e4", 125, [1, 1, 30, 8], [500, 3, 100, 8], kv_dtype="fp8",
+                               k_scale=0.05, v_scale=0.07, head_dim=256, num_q_heads=8,
+                               num_kv_heads=2)),
+    ("d256_fp8_per_head_p64", lambda: _case("e5", 126, [1, 1, 70], [900, 64, 200],
+                                            kv_dtype="fp8", head_dim=256, page_size=64,
+                                            k_scale_heads=[0.04, 0.1], v_scale_heads=[0.06, 0.02],
+                                            has_sink=True)),
+    ("d256_g16_p4", lambda: _case("e6", 127, [1, 1, 20], [260, 7, 45], num_q_heads=32,
+                                  num_kv_heads=2, head_dim=256, page_size=4)),
 ]
 
 
@@ -291,15 +311,27 @@ def test_bad_per_head_scale_sets_status():
     assert status == _lib.RPA_STATUS_BAD_SCALE
 
 
-def test_decode_units_fill_the_workspace_bound():
+@pytest.mark.parametrize("head_dim", [64, 128, 256])
+def test_decode_units_fill_the_workspace_bound(head_dim):
     """65 decode sequences x 8 kv heads, window 1000 starting 63 keys into a
     64-key stage: with the split target of 512 the chunk is 1024 keys and
     every (sequence, head) spans 1063 keys, so each takes two splits -- 1040
     units, more than target + sequences * heads.  The workspace must hold them
-    and the results must match the oracle."""
+    and the results must match the oracle.  Half the units are one-stage tails,
+    so the producer often waits on a query slot while the consumers still read
+    it: three runs must give bit-identical outputs (the split combine reads the
+    partials in a fixed order, so any difference is a race)."""
     S = 65
     kv = [1063 + 64 * (s % 4) for s in range(S)]
-    check_case(_case("wb", 137, [1] * S, kv, num_q_heads=8, num_kv_heads=8, sliding_window=1000))
+    w = _case("wb", 137, [1] * S, kv, num_q_heads=8, num_kv_heads=8, sliding_window=1000,
+              head_dim=head_dim)
+    first, _ = check_case(w)
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu")
+    for _ in range(2):
+        again, _, status = run_gpu(w, q, k, v, pool)
+        assert status == 0
+        assert np.array_equal(again[:S], first), "decode output differs between runs"
 
 
 def test_empty_batch_is_a_no_op():

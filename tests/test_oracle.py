@@ -124,6 +124,8 @@ SMALL_CASES = [
                                     k_scale_heads=[0.02, 0.09, 0.3],
                                     v_scale_heads=[0.15, 0.04, 0.011], has_sink=True)),
     ("q_len0", lambda: _small("g", 17, [0, 4, 0], [5, 4, 11])),
+    ("d256", lambda: _small("h", 19, [1, 6, 2], [23, 6, 9], head_dim=256, num_q_heads=4,
+                            num_kv_heads=2, logits_soft_cap=50.0, sliding_window=8)),
 ]
 
 
