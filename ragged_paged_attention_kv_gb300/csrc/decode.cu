@@ -36,10 +36,14 @@ constexpr int kRescaleLog2 = 8;               // lazy-rescale threshold (log2 un
 
 template <int D, bool FP8>
 struct Cfg {
-  // head_dim 64 fits two CTAs per SM (registers and shared memory), which
-  // doubles the units in flight when short units make the path
-  // latency-bound; the per-SM ring depth stays the same
-  static constexpr int kCtasPerSm = D == 64 ? 2 : 1;
+  // Two CTAs per SM put two consumer warps on each scheduler, so one warp's
+  // ldmatrix -> MMA -> softmax chain hides behind the other's, and double the
+  // units in flight when short units make the path latency-bound.  head_dim
+  // 64 fits them outright; bf16 head_dim 128 fits in 168 registers (12 bytes
+  // of spills) and two 32 KB stages per CTA (128 KB in flight per SM), and
+  // runs 4 % faster than one CTA with five stages.  fp8 at 128 (more
+  // conversion registers) and head_dim 256 keep one CTA per SM.
+  static constexpr int kCtasPerSm = (D == 64 || (D == 128 && !FP8)) ? 2 : 1;
   static constexpr int kRowBytes = FP8 ? D : 128;        // bytes of one box row in smem
   static constexpr int kHalves = FP8 ? 1 : D / 64;       // boxes across head_dim
   // a stage holds, per 64-wide half of head_dim, 2*kBN rows: key j at row 2j,
