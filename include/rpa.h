@@ -76,8 +76,10 @@ extern "C" {
 #define RPA_OK 0
 #define RPA_ERR_INVALID_ARG 1  /* null pointer, negative size, bad scale,
                                   per-head scales with a bf16 cache        */
-#define RPA_ERR_UNSUPPORTED 2  /* head_dim not 64/128/256, Hq/Hkv not in {1,2,4,8,16},
-                                  page_size not a power of two in [1,1024] */
+#define RPA_ERR_UNSUPPORTED 2  /* head_dim not 64/96/128/192/256, Hq/Hkv not in {1,2,4,8,16},
+                                  page_size not a power of two in [1,1024],
+                                  or an fp8 cache with head_dim 64/96 and
+                                  page_size 1 */
 #define RPA_ERR_WORKSPACE 3    /* workspace NULL, misaligned or too small   */
 #define RPA_ERR_CUDA 4         /* a CUDA runtime call failed                */
 
@@ -96,7 +98,7 @@ typedef enum { RPA_KV_BF16 = 0, RPA_KV_FP8_E4M3 = 1 } rpa_kv_dtype_t;
 typedef struct {
   int32_t num_q_heads;    /* Hq; Hq % Hkv == 0                              */
   int32_t num_kv_heads;   /* Hkv                                            */
-  int32_t head_dim;       /* D: 64, 128 or 256                              */
+  int32_t head_dim;       /* D: 64, 96, 128, 192 or 256                     */
   int32_t page_size;      /* P: power of two, 1..1024                       */
   int32_t num_pages;      /* pages in the pool                              */
   int32_t pages_per_seq;  /* row length of block_tables                     */

@@ -22,11 +22,15 @@ static int check_params(const rpa_params_t* p) {
   if (p->num_q_heads % p->num_kv_heads != 0) return RPA_ERR_UNSUPPORTED;
   const int G = p->num_q_heads / p->num_kv_heads;
   if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16)) return RPA_ERR_UNSUPPORTED;
-  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return RPA_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 96 && p->head_dim != 128 && p->head_dim != 192 &&
+      p->head_dim != 256)
+    return RPA_ERR_UNSUPPORTED;
   if (!is_pow2(p->page_size) || p->page_size > 1024) return RPA_ERR_UNSUPPORTED;
   if (p->kv_dtype != RPA_KV_BF16 && p->kv_dtype != RPA_KV_FP8_E4M3) return RPA_ERR_UNSUPPORTED;
-  // fp8 rows of 64 bytes need at least two rows per page for 128-byte aligned copies
-  if (p->kv_dtype == RPA_KV_FP8_E4M3 && p->head_dim == 64 && p->page_size < 2)
+  // fp8 rows of 64 or 96 bytes need at least two rows per page for 128-byte
+  // aligned copies
+  if (p->kv_dtype == RPA_KV_FP8_E4M3 && (p->head_dim == 64 || p->head_dim == 96) &&
+      p->page_size < 2)
     return RPA_ERR_UNSUPPORTED;
   if (!(p->softmax_scale > 0.f) || !(p->logits_soft_cap >= 0.f))
     return RPA_ERR_INVALID_ARG;

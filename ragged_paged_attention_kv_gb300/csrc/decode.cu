@@ -43,22 +43,31 @@ struct Cfg {
   // of spills) and two 32 KB stages per CTA (128 KB in flight per SM), and
   // runs 4 % faster than one CTA with five stages.  fp8 at 128 (more
   // conversion registers) and head_dim 256 keep one CTA per SM.
-  static constexpr int kCtasPerSm = (D == 64 || (D == 128 && !FP8)) ? 2 : 1;
-  static constexpr int kRowBytes = FP8 ? D : 128;        // bytes of one box row in smem
-  static constexpr int kHalves = FP8 ? 1 : D / 64;       // boxes across head_dim
+  // head_dim 96 runs as 128 in shared memory (a multiple of 64 columns):
+  // past the real row, bf16 stages hold TMA's zero fill and fp8 ones the
+  // conversion's zeros; the query rows land at the padded stride; only the
+  // real columns are read from or written to global memory
+  static constexpr int kDp = (D + 63) / 64 * 64;
+  static constexpr int kCtasPerSm = (kDp == 64 || (kDp == 128 && !FP8)) ? 2 : 1;
+  // bytes of one box row in smem: an fp8 stage keeps the real head_dim (the
+  // conversion to the padded bf16 operand zero-fills the rest)
+  static constexpr int kRowBytes = FP8 ? D : 128;
+  static constexpr int kHalves = FP8 ? 1 : kDp / 64;     // 64-column boxes of a stage
   // a stage holds, per 64-wide half of head_dim, 2*kBN rows: key j at row 2j,
   // value j at row 2j+1 (one TMA box brings both for a page)
   static constexpr int kHalfBytes = 2 * kBN * kRowBytes;
   static constexpr int kStageBytes = kHalves * kHalfBytes;
-  // head_dim 256: the query fragments (64 registers) are re-read from the
-  // slot every stage instead of being held, and each row lands with its own
-  // bulk copy at a 16-byte padded stride, so those ldmatrix reads are free
-  // of bank conflicts; the slot is then released at the end of the unit
-  static constexpr bool kQFromSmem = D > 128;
-  static constexpr int kQRow = kQFromSmem ? D * 2 + 16 : D * 2;  // bytes per query row
+  // head_dim 192 and 256: the query fragments (48 / 64 registers) are
+  // re-read from the slot every stage instead of being held, and each row
+  // lands with its own bulk copy at a 16-byte padded stride, so those
+  // ldmatrix reads are free of bank conflicts; the slot is then released at
+  // the end of the unit
+  static constexpr bool kQFromSmem = kDp > 128;
+  static constexpr int kQRow = kQFromSmem ? kDp * 2 + 16 : kDp * 2;  // bytes per query row
+  static constexpr bool kQPerRow = kQFromSmem || D != kDp;  // one bulk copy per query row
   static constexpr int kQBytes = kDecodeRows * kQRow;    // one query slot
-  static constexpr int kConvBytes = FP8 ? kConsumerWarps * 2 * kKeysPerWarp * D * 2 : 0;
-  static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * (D + 2) * 4;
+  static constexpr int kConvBytes = FP8 ? kConsumerWarps * 2 * kKeysPerWarp * kDp * 2 : 0;
+  static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * (kDp + 2) * 4;
   // as many stages as fit next to the other buffers (at most 12, 160 KB)
   static constexpr int kBudget =
       (kCtasPerSm == 2 ? 110 : 220) * 1024 - 2 * kQBytes - kConvBytes - kMergeBytes - 1024 - 256;
@@ -96,6 +105,7 @@ template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
     decode_kernel(const __grid_constant__ DecodeMaps maps, AttnArgs a) {
   using C = Cfg<D, FP8>;
+  constexpr int Dp = C::kDp;  // head_dim as laid out in shared memory
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -203,12 +213,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         info[slot] = ui;
         const uint32_t qbytes = (uint32_t)(G * D * 2);
         mbar_arrive_expect_tx(bar_qfull + 8 * slot, qbytes);
-        if (!C::kQFromSmem)
+        if (!C::kQPerRow)
           bulk_load(s_base + C::kOffQ + slot * C::kQBytes,
                     a.queries + ((int64_t)q0 * p.num_q_heads + du.head * G) * D, qbytes,
                     bar_qfull + 8 * slot);
       }
-      if (C::kQFromSmem) {  // one row per lane at the padded stride
+      if (C::kQPerRow) {  // one row per lane at the padded stride
         __syncwarp();       // the expected bytes are posted first
         if (lane < G)
           bulk_load(s_base + C::kOffQ + slot * C::kQBytes + lane * C::kQRow,
@@ -287,10 +297,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       const int col = (2 * ks + (mi >> 1)) * 16;
       ldmatrix_x4(sq + row * C::kQRow + col, f[0], f[1], f[2], f[3]);
     };
-    uint32_t qa[C::kQFromSmem ? 1 : D / 16][4];
+    uint32_t qa[C::kQFromSmem ? 1 : Dp / 16][4];
     if constexpr (!C::kQFromSmem) {
 #pragma unroll
-      for (int ks = 0; ks < (C::kQFromSmem ? 1 : D / 16); ++ks) load_q(ks, qa[ks]);
+      for (int ks = 0; ks < (C::kQFromSmem ? 1 : Dp / 16); ++ks) load_q(ks, qa[ks]);
       // The slot is refilled by a bulk copy (async proxy) once all warps
       // have arrived, and nothing reads qa before the first stage lands, so
       // the ldmatrix reads may still be in flight here: a proxy fence orders
@@ -301,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       if (lane == 0) mbar_arrive(bar_qempty + 8 * slot);
     }
 
-    float o[D / 8][4];
+    float o[Dp / 8][4];
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int n = 0; n < Dp / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
     const int kb0 = du.k_begin & ~(kBN - 1);
@@ -322,18 +332,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       if (FP8) {
         // convert this warp's 16 keys/values to bf16 in its own buffer; keys
         // outside the unit become zero, the new token comes from the inputs
-        const uint32_t cK = s_base + C::kOffConv + warp * 2 * kKeysPerWarp * D * 2;
-        const uint32_t cV = cK + kKeysPerWarp * D * 2;
+        const uint32_t cK = s_base + C::kOffConv + warp * 2 * kKeysPerWarp * Dp * 2;
+        const uint32_t cV = cK + kKeysPerWarp * Dp * 2;
         uint8_t* gK = smem + (cK - s_base);
         uint8_t* gV = smem + (cV - s_base);
-        for (int idx = lane; idx < 2 * kKeysPerWarp * (D / 8); idx += 32) {
-          const int kv = idx / (kKeysPerWarp * (D / 8));
-          const int rem = idx % (kKeysPerWarp * (D / 8));
-          const int r = rem / (D / 8), c = rem % (D / 8);
+        for (int idx = lane; idx < 2 * kKeysPerWarp * (Dp / 8); idx += 32) {
+          const int kv = idx / (kKeysPerWarp * (Dp / 8));
+          const int rem = idx % (kKeysPerWarp * (Dp / 8));
+          const int r = rem / (Dp / 8), c = rem % (Dp / 8);
           const int j = kw + r;
           uint4 val;
-          if (j < du.k_begin || j >= du.k_end) {
-            val = make_uint4(0, 0, 0, 0);
+          if (j < du.k_begin || j >= du.k_end || c >= D / 8) {
+            val = make_uint4(0, 0, 0, 0);  // masked key, or a padding column
           } else if (j == ctx) {
             const __nv_bfloat16* in = (kv ? a.kv.values : a.kv.keys) +
                                       ((int64_t)q0 * p.num_kv_heads + h) * D + c * 8;
@@ -344,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
                 smem + (stage - s_base) + (2 * (warp * kKeysPerWarp + r) + kv) * C::kRowBytes + c * 8);
             val = dequant8(codes);
           }
-          *reinterpret_cast<uint4*>((kv ? gV : gK) + swz(r, c, D * 2)) = val;
+          *reinterpret_cast<uint4*>((kv ? gV : gK) + swz(r, c, Dp * 2)) = val;
         }
         __syncwarp();
         tK = cK;
@@ -359,13 +369,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         const bool edge = kw < du.k_begin || kw + kKeysPerWarp > du.k_end ||
                           (ctx >= kw && ctx < kw + kKeysPerWarp);
         if (edge) {
-          for (int idx = lane; idx < kKeysPerWarp * (D / 8); idx += 32) {
-            const int r = idx / (D / 8), c = idx % (D / 8);
+          for (int idx = lane; idx < kKeysPerWarp * (Dp / 8); idx += 32) {
+            const int r = idx / (Dp / 8), c = idx % (Dp / 8);
             const int j = kw + r;
             if (j < du.k_begin || j >= du.k_end) {
               *reinterpret_cast<uint4*>(smem + (kv_addr(stage, krow0 + r, 1, c) - s_base)) =
                   make_uint4(0, 0, 0, 0);
-            } else if (j == ctx) {
+            } else if (j == ctx && c < D / 8) {  // its padding columns hold TMA's zeros
               const int64_t off = ((int64_t)q0 * p.num_kv_heads + h) * D + c * 8;
               *reinterpret_cast<uint4*>(smem + (kv_addr(stage, krow0 + r, 0, c) - s_base)) =
                   __ldg(reinterpret_cast<const uint4*>(a.kv.keys + off));
@@ -382,11 +392,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
 #pragma unroll
       for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
+      for (int ks = 0; ks < Dp / 16; ++ks) {
         const int mi = lane >> 3;
         const int key = krow0 + (lane & 7) + ((mi >> 1) << 3);
         const int chunk = 2 * ks + (mi & 1);
-        const uint32_t addr = FP8 ? tK + swz(key, chunk, D * 2) : kv_addr(tK, key, 0, chunk);
+        const uint32_t addr = FP8 ? tK + swz(key, chunk, Dp * 2) : kv_addr(tK, key, 0, chunk);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(addr, b0, b1, b2, b3);
         if constexpr (C::kQFromSmem) {
@@ -435,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         }
       if (rescale) {
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
+        for (int n = 0; n < Dp / 8; ++n) {
           o[n][0] *= alpha[0];
           o[n][1] *= alpha[0];
           o[n][2] *= alpha[1];
@@ -450,11 +460,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       pa[2] = pack_bf16(sc[1][0], sc[1][1]);
       pa[3] = pack_bf16(sc[1][2], sc[1][3]);
 #pragma unroll
-      for (int cp = 0; cp < D / 16; ++cp) {
+      for (int cp = 0; cp < Dp / 16; ++cp) {
         const int mi = lane >> 3;
         const int key = krow0 + (lane & 7) + ((mi & 1) << 3);
         const int chunk = 2 * cp + (mi >> 1);
-        const uint32_t addr = FP8 ? tV + swz(key, chunk, D * 2) : kv_addr(tV, key, 1, chunk);
+        const uint32_t addr = FP8 ? tV + swz(key, chunk, Dp * 2) : kv_addr(tV, key, 1, chunk);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(addr, b0, b1, b2, b3);
         mma_bf16_16816(o[2 * cp], pa, b0, b1);
@@ -483,17 +493,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
     // the G rows of the GQA group are real, the rest of the 16-row tile is
     // padding and is not stored
     {
-      float* mw = sMerge + warp * kDecodeRows * (D + 2);
+      float* mw = sMerge + warp * kDecodeRows * (Dp + 2);
       const float l0 = quad_sum(l_run[0]), l1 = quad_sum(l_run[1]);
       if (gq < G) {
-        float* row = mw + gq * (D + 2);
+        float* row = mw + gq * (Dp + 2);
         if (tq == 0) *reinterpret_cast<float2*>(row) = make_float2(m_run[0], l0);
 #pragma unroll
         for (int n = 0; n < D / 8; ++n)
           *reinterpret_cast<float2*>(row + 2 + n * 8 + 2 * tq) = make_float2(o[n][0], o[n][1]);
       }
       if (gq + 8 < G) {
-        float* row = mw + (gq + 8) * (D + 2);
+        float* row = mw + (gq + 8) * (Dp + 2);
         if (tq == 0) *reinterpret_cast<float2*>(row) = make_float2(m_run[1], l1);
 #pragma unroll
         for (int n = 0; n < D / 8; ++n)
@@ -508,11 +518,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       const int r = idx / (D / 4), d = (idx % (D / 4)) * 4;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sMerge[(w * kDecodeRows + r) * (D + 2)]);
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sMerge[(w * kDecodeRows + r) * (Dp + 2)]);
       float Lsum = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float* row = sMerge + (w * kDecodeRows + r) * (D + 2);
+        const float* row = sMerge + (w * kDecodeRows + r) * (Dp + 2);
         const float scw = row[0] == -INFINITY ? 0.f : exp2f(row[0] - M);
         Lsum += scw * row[1];
 #pragma unroll
@@ -599,6 +609,8 @@ static cudaError_t launch_decode_t(const AttnArgs& a, int max_units, int num_sms
   const rpa_params_t& p = a.kv.p;
   dec::DecodeMaps maps;
   const uint32_t rows = p.page_size < dec::kBN ? (uint32_t)p.page_size : (uint32_t)dec::kBN;
+  // bf16 boxes are 64 columns wide (at head_dim 96 the second one reads TMA's
+  // zero fill past the row); an fp8 box spans the real row
   if (!encode_map_3d(&maps.cache, a.kv.cache, FP8 ? 1 : 2, (uint64_t)D,
                      2 * (uint64_t)p.num_kv_heads, (uint64_t)p.num_pages * p.page_size,
                      FP8 ? (uint32_t)D : 64u, 2u, rows, !FP8))
@@ -615,6 +627,12 @@ cudaError_t launch_decode(const AttnArgs& a, int max_units, int num_sms, cudaStr
   if (a.kv.p.head_dim == 64)
     return fp8 ? launch_decode_t<64, true>(a, max_units, num_sms, stream)
                : launch_decode_t<64, false>(a, max_units, num_sms, stream);
+  if (a.kv.p.head_dim == 96)
+    return fp8 ? launch_decode_t<96, true>(a, max_units, num_sms, stream)
+               : launch_decode_t<96, false>(a, max_units, num_sms, stream);
+  if (a.kv.p.head_dim == 192)
+    return fp8 ? launch_decode_t<192, true>(a, max_units, num_sms, stream)
+               : launch_decode_t<192, false>(a, max_units, num_sms, stream);
   if (a.kv.p.head_dim == 256)
     return fp8 ? launch_decode_t<256, true>(a, max_units, num_sms, stream)
                : launch_decode_t<256, false>(a, max_units, num_sms, stream);

@@ -13,7 +13,7 @@ cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int
 cudaError_t launch_cache_write(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,
                                int prefill_rows, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
-// warp-level MMA prefill (64-row tiles): pages of fewer than 8 rows, and head_dim 256
+// warp-level MMA prefill (64-row tiles): pages of fewer than 8 rows, and head_dim 96/192/256
 cudaError_t launch_prefill(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
 // tcgen05 prefill (two 128-row query tiles per unit): head_dim 64 and 128, pages >= 8 rows
 bool prefill_uses_tc(const rpa_params_t& p);

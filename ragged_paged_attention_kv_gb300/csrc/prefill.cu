@@ -26,7 +26,8 @@ constexpr int kStages = 2;
 
 template <int D>
 struct Smem {
-  static constexpr int kRowBytes = D * 2;  // tiles are held as bf16
+  static constexpr int kDp = (D + 63) / 64 * 64;  // head_dim 96 runs as 128 (zero columns)
+  static constexpr int kRowBytes = kDp * 2;        // tiles are held as bf16
   static constexpr int kQBytes = kBM * kRowBytes;
   static constexpr int kStageBytes = 2 * kBN * kRowBytes;
   static constexpr int kBytes = kQBytes + kStages * kStageBytes;
@@ -36,15 +37,16 @@ struct Smem {
 template <int D, bool FP8>
 __device__ __forceinline__ void load_tile(const AttnArgs& a, uint8_t* stage, int seq, int h,
                                           int kb, int lo, int hi, int ctx, int q0, int tid) {
-  constexpr int kChunks = D / 8;  // 16-byte bf16 chunks per row
+  constexpr int kDp = Smem<D>::kDp;
+  constexpr int kChunks = kDp / 8;  // 16-byte bf16 chunks per padded row
   const int Hkv = a.kv.p.num_kv_heads;
   for (int idx = tid; idx < kBN * 2 * kChunks; idx += kThreads) {
     const int key = idx / (2 * kChunks);
     const int rem = idx % (2 * kChunks);
     const int kv = rem / kChunks, c = rem % kChunks;
     const int j = kb + key;
-    uint8_t* dst = stage + kv * kBN * (D * 2) + swz(key, c, D * 2);
-    if (j < lo || j > hi) {
+    uint8_t* dst = stage + kv * kBN * (kDp * 2) + swz(key, c, kDp * 2);
+    if (j < lo || j > hi || c >= D / 8) {  // masked key, or a padding column
       *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
       continue;
     }
@@ -79,6 +81,7 @@ __device__ __forceinline__ void load_tile(const AttnArgs& a, uint8_t* stage, int
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
   using S = Smem<D>;
+  constexpr int Dp = S::kDp;  // head_dim as laid out in shared memory
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* sQ = smem;
   uint8_t* sStages = smem + S::kQBytes;
@@ -115,11 +118,11 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
       write_token_kv<FP8>(a.kv, seq, q0 + pu.t_begin + i, ctx + pu.t_begin + i, h, lane);
 
     // Q tile (rows past the tile's tokens are zero)
-    for (int idx = tid; idx < kBM * (D / 8); idx += kThreads) {
-      const int r = idx / (D / 8), c = idx % (D / 8);
+    for (int idx = tid; idx < kBM * (Dp / 8); idx += kThreads) {
+      const int r = idx / (Dp / 8), c = idx % (Dp / 8);
       const int ti = r / G;
-      uint8_t* dst = sQ + swz(r, c, D * 2);
-      if (ti < n_tok) {
+      uint8_t* dst = sQ + swz(r, c, Dp * 2);
+      if (ti < n_tok && c < D / 8) {
         const int t = q0 + pu.t_begin + ti;
         cp_async_16(smem_u32(dst), a.queries + ((int64_t)t * p.num_q_heads + h * G + r % G) * D + c * 8);
       } else {
@@ -143,21 +146,21 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
       rpos[r] = ctx + pu.t_begin + ti;
     }
 
-    float o[D / 8][4];
+    float o[Dp / 8][4];
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int n = 0; n < Dp / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     // query fragment ks of this warp's 16 rows; up to head_dim 128 they are
     // held in registers for the whole unit, at 256 (64 registers) they are
     // re-read from the swizzled Q tile for every key tile
-    constexpr bool kQFromSmem = D > 128;
+    constexpr bool kQFromSmem = Dp > 128;
     auto load_q = [&](int ks, uint32_t (&f)[4]) {
       const int mi = lane >> 3;
       const int row = warp * 16 + (lane & 7) + ((mi & 1) << 3);
       const int chunk = 2 * ks + (mi >> 1);
-      ldmatrix_x4(smem_u32(sQ + swz(row, chunk, D * 2)), f[0], f[1], f[2], f[3]);
+      ldmatrix_x4(smem_u32(sQ + swz(row, chunk, Dp * 2)), f[0], f[1], f[2], f[3]);
     };
-    uint32_t qa[kQFromSmem ? 1 : D / 16][4];
+    uint32_t qa[kQFromSmem ? 1 : Dp / 16][4];
 
     for (int kt = 0; kt < n_kt; ++kt) {
       if (kt + 1 < n_kt)
@@ -169,18 +172,18 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
       if constexpr (!kQFromSmem) {
         if (kt == 0) {
 #pragma unroll
-          for (int ks = 0; ks < (kQFromSmem ? 1 : D / 16); ++ks) load_q(ks, qa[ks]);
+          for (int ks = 0; ks < (kQFromSmem ? 1 : Dp / 16); ++ks) load_q(ks, qa[ks]);
         }
       }
       const uint8_t* tK = sStages + (kt % kStages) * S::kStageBytes;
-      const uint8_t* tV = tK + kBN * (D * 2);
+      const uint8_t* tV = tK + kBN * (Dp * 2);
       const int kb = lo + kt * kBN;
 
       float s[kBN / 8][4];
 #pragma unroll
       for (int n = 0; n < kBN / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
+      for (int ks = 0; ks < Dp / 16; ++ks) {
         uint32_t qf[4];
         if constexpr (kQFromSmem) {
           load_q(ks, qf);
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
           const int key = np * 16 + (lane & 7) + ((mi >> 1) << 3);
           const int chunk = 2 * ks + (mi & 1);
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(smem_u32(tK + swz(key, chunk, D * 2)), b0, b1, b2, b3);
+          ldmatrix_x4(smem_u32(tK + swz(key, chunk, Dp * 2)), b0, b1, b2, b3);
           mma_bf16_16816(s[2 * np], qf, b0, b1);
           mma_bf16_16816(s[2 * np + 1], qf, b2, b3);
         }
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + rs[r];
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
+      for (int n = 0; n < Dp / 8; ++n) {
         o[n][0] *= alpha[0];
         o[n][1] *= alpha[0];
         o[n][2] *= alpha[1];
@@ -252,12 +255,12 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
         pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
         pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
 #pragma unroll
-        for (int cp = 0; cp < D / 16; ++cp) {
+        for (int cp = 0; cp < Dp / 16; ++cp) {
           const int mi = lane >> 3;
           const int key = kk * 16 + (lane & 7) + ((mi & 1) << 3);
           const int chunk = 2 * cp + (mi >> 1);
           uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(smem_u32(tV + swz(key, chunk, D * 2)), b0, b1, b2, b3);
+          ldmatrix_x4_trans(smem_u32(tV + swz(key, chunk, Dp * 2)), b0, b1, b2, b3);
           mma_bf16_16816(o[2 * cp], pa, b0, b1);
           mma_bf16_16816(o[2 * cp + 1], pa, b2, b3);
         }
@@ -327,6 +330,12 @@ cudaError_t launch_prefill(const AttnArgs& a, int max_units, int num_sms, cudaSt
   if (a.kv.p.head_dim == 64)
     return fp8 ? launch_prefill_t<64, true>(a, max_units, num_sms, stream)
                : launch_prefill_t<64, false>(a, max_units, num_sms, stream);
+  if (a.kv.p.head_dim == 96)
+    return fp8 ? launch_prefill_t<96, true>(a, max_units, num_sms, stream)
+               : launch_prefill_t<96, false>(a, max_units, num_sms, stream);
+  if (a.kv.p.head_dim == 192)
+    return fp8 ? launch_prefill_t<192, true>(a, max_units, num_sms, stream)
+               : launch_prefill_t<192, false>(a, max_units, num_sms, stream);
   if (a.kv.p.head_dim == 256)
     return fp8 ? launch_prefill_t<256, true>(a, max_units, num_sms, stream)
                : launch_prefill_t<256, false>(a, max_units, num_sms, stream);

@@ -68,7 +68,7 @@ def test_workspace_size_host_only(lib):
     assert workspace_size(_params(total_tokens=65536, max_num_seqs=2)) > 0
 
 
-@pytest.mark.parametrize("head_dim", [64, 128, 256])
+@pytest.mark.parametrize("head_dim", [64, 96, 128, 192, 256])
 def test_supported_head_dims(lib, head_dim):
     n = ctypes.c_size_t(0)
     p = _params(head_dim=head_dim)
@@ -76,9 +76,10 @@ def test_supported_head_dims(lib, head_dim):
 
 
 @pytest.mark.parametrize("over,code", [
-    (dict(head_dim=96), 2),
-    (dict(head_dim=192), 2),
+    (dict(head_dim=80), 2),
+    (dict(head_dim=160), 2),
     (dict(head_dim=512), 2),
+    (dict(kv_fp8=True, head_dim=96, page_size=1), 2),  # 96-byte fp8 rows need 2-row pages
     (dict(num_q_heads=24, num_kv_heads=8), 2),
     (dict(num_q_heads=30, num_kv_heads=8), 2),
     (dict(page_size=24), 2),

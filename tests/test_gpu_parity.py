@@ -154,6 +154,22 @@ CASES = [
                                             has_sink=True)),
     ("d256_g16_p4", lambda: _case("e6", 127, [1, 1, 20], [260, 7, 45], num_q_heads=32,
                                   num_kv_heads=2, head_dim=256, page_size=4)),
+    # head_dim 96 (run as 128 with zero columns) and 192 (three 64-column blocks)
+    ("d96_decode_prefill", lambda: _case("e7", 128, [1, 1, 1, 40, 9], [700, 17, 300, 140, 9],
+                                         num_q_heads=32, num_kv_heads=8, head_dim=96,
+                                         distribution=[3, 4, 5])),
+    ("d96_mha_options", lambda: _case("e8", 129, [1, 1, 33], [1290, 2, 120], num_q_heads=4,
+                                      num_kv_heads=4, head_dim=96, sliding_window=100,
+                                      logits_soft_cap=30.0, has_sink=True)),
+    ("d96_fp8", lambda: _case("e9", 130, [1, 1, 30, 8], [500, 3, 100, 8], kv_dtype="fp8",
+                              k_scale=0.05, v_scale=0.07, head_dim=96)),
+    ("d96_p1", lambda: _case("e10", 131, [1, 6], [40, 20], head_dim=96, page_size=1)),
+    ("d192_decode_prefill", lambda: _case("e11", 132, [1, 1, 70, 5], [900, 64, 200, 260],
+                                          num_q_heads=16, num_kv_heads=4, head_dim=192)),
+    ("d192_fp8_options", lambda: _case("e12", 133, [1, 1, 20], [600, 33, 45], kv_dtype="fp8",
+                                       head_dim=192, k_scale_heads=[0.04, 0.1],
+                                       v_scale_heads=[0.06, 0.02], logits_soft_cap=20.0,
+                                       sliding_window=150, page_size=32)),
 ]
 
 
@@ -311,7 +327,7 @@ def test_bad_per_head_scale_sets_status():
     assert status == _lib.RPA_STATUS_BAD_SCALE
 
 
-@pytest.mark.parametrize("head_dim", [64, 128, 256])
+@pytest.mark.parametrize("head_dim", [64, 96, 128, 192, 256])
 def test_decode_units_fill_the_workspace_bound(head_dim):
     """65 decode sequences x 8 kv heads, window 1000 starting 63 keys into a
     64-key stage: with the split target of 512 the chunk is 1024 keys and

@@ -126,6 +126,8 @@ SMALL_CASES = [
     ("q_len0", lambda: _small("g", 17, [0, 4, 0], [5, 4, 11])),
     ("d256", lambda: _small("h", 19, [1, 6, 2], [23, 6, 9], head_dim=256, num_q_heads=4,
                             num_kv_heads=2, logits_soft_cap=50.0, sliding_window=8)),
+    ("d96_fp8", lambda: _small("i", 20, [1, 5], [17, 5], head_dim=96, kv_dtype="fp8",
+                               k_scale=0.05, v_scale=0.07)),
 ]
 
 
