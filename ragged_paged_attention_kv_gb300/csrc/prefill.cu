@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
     for (int n = 0; n < Dp / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     // query fragment ks of this warp's 16 rows; up to head_dim 128 they are
-    // held in registers for the whole unit, at 256 (64 registers) they are
-    // re-read from the swizzled Q tile for every key tile
+    // held in registers for the whole unit, from 192 on (48 / 64 registers)
+    // they are re-read from the swizzled Q tile for every key tile
     constexpr bool kQFromSmem = Dp > 128;
     auto load_q = [&](int ks, uint32_t (&f)[4]) {
       const int mi = lane >> 3;
