@@ -15,9 +15,7 @@
 
 namespace rpa {
 
-constexpr int kPlanThreads = 1024;
 constexpr int kSizeClasses = 16;  // decode sequences are ordered by these, longest first
-static_assert((kSizeClasses + 1) * 32 <= kPlanThreads, "one scan covers the class counts");
 
 // Block-wide exclusive scan of two ints per thread (one set of barriers for
 // both); returns the prefixes and writes the block totals to *total.  All
@@ -107,16 +105,20 @@ __device__ SeqPlan classify(const rpa_params_t& p, int s, int d0, const SeqMeta&
   return sp;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, const int32_t* kv_lens,
+// kT threads (256 or 1024) handle the sequences in batches of kT; fewer
+// threads make the block's barriers cheaper when the batch is small.
+template <int kT>
+__global__ void __launch_bounds__(kT) plan_kernel(rpa_params_t p, const int32_t* kv_lens,
                                                             const int32_t* qsl,
                                                             const int32_t* dist, int32_t* ws,
                                                             int prefill_rows) {
   __shared__ int s_flags;
   __shared__ int2 s_scan[33];
   __shared__ unsigned long long s_keys;
-  __shared__ int s_doff[kPlanThreads], s_poff[kPlanThreads], s_nsplit[kPlanThreads],
-      s_ntiles[kPlanThreads], s_lo[kPlanThreads], s_len[kPlanThreads], s_q0[kPlanThreads],
-      s_seq[kPlanThreads], s_wbase[kPlanThreads];
+  constexpr int kWarps = kT / 32;
+  static_assert((kSizeClasses + 1) * kWarps <= kT, "one scan covers the class counts");
+  __shared__ int s_doff[kT], s_poff[kT], s_nsplit[kT], s_ntiles[kT], s_lo[kT], s_len[kT],
+      s_q0[kT], s_seq[kT], s_wbase[kT];
   __shared__ int s_maxkey;
   const WorkspaceLayout L(p);
   DecodeUnit* dunits = reinterpret_cast<DecodeUnit*>(reinterpret_cast<char*>(ws) + L.decode_units_off);
@@ -131,13 +133,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   // (every index below max_num_seqs is inside the arrays)
   SeqMeta meta0{0, 0, 0};
   if (tid < p.max_num_seqs) meta0 = load_meta(tid, kv_lens, qsl);
+  const int d0 = __ldg(dist), d1 = __ldg(dist + 1), d2 = __ldg(dist + 2);
   if (tid == 0) {
     s_flags = 0;
     s_keys = 0ull;
     s_maxkey = 0;
   }
   __syncthreads();
-  const int d0 = dist[0], d1 = dist[1], d2 = dist[2];
   int S = d2;
   if (!(0 <= d0 && d0 <= d1 && d1 <= d2 && d2 <= p.max_num_seqs)) {
     if (tid == 0) atomicOr(&s_flags, RPA_STATUS_BAD_DISTRIBUTION);
@@ -146,7 +148,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   if (tid == 0 && S > 0 && meta0.a != 0) atomicOr(&s_flags, RPA_STATUS_BAD_QUERY_START_LOC);
   // per-head scales must be finite and positive
   if (p.k_scale_heads || p.v_scale_heads) {
-    for (int h = tid; h < Hkv; h += kPlanThreads) {
+    for (int h = tid; h < Hkv; h += kT) {
       const float ks = p.k_scale_heads ? __ldg(p.k_scale_heads + h) : 1.f;
       const float vs = p.v_scale_heads ? __ldg(p.v_scale_heads + h) : 1.f;
       if (!(ks > 0.f && ks <= FLT_MAX && vs > 0.f && vs <= FLT_MAX))
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   // Pass 1: total decode keys (per kv head) to size the splits.
   unsigned long long my_keys = 0;
   int my_max = 0;
-  for (int s = tid; s < S; s += kPlanThreads) {
+  for (int s = tid; s < S; s += kT) {
     SeqPlan sp = classify(p, s, d0, s == tid ? meta0 : load_meta(s, kv_lens, qsl));
     if (sp.flags) atomicOr(&s_flags, sp.flags);
     if (sp.cls == 1) {
@@ -178,13 +180,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
   int chunk = (int)((want + 63) / 64 * 64);
   if (chunk < kDecodeChunkMin) chunk = kDecodeChunkMin;
 
-  // Pass 2, per batch of kPlanThreads sequences: scan the unit counts, then
+  // Pass 2, per batch of kT sequences: scan the unit counts, then
   // emit the units cooperatively (one thread per unit, coalesced stores).
   // Prefill units are ordered head-major, each head's tiles last-first, so the
   // CTAs running at the same time share one head's keys in L2 and the longest
   // causal tiles start first under the dynamic scheduler.
   int dec_base = 0, pf_base = 0;
-  for (int base = 0; base < S; base += kPlanThreads) {
+  for (int base = 0; base < S; base += kT) {
     const int s = base + tid;
     SeqPlan sp{0, 0, 0, 0, 0, 0};
     int nsplit = 0, ntiles = 0;
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
       const int lane = tid & 31, warp = tid >> 5;
       s_wbase[tid] = 0;
       __syncthreads();
-      if (lane == __ffs(same) - 1) s_wbase[kb * 32 + warp] = __popc(same);
+      if (lane == __ffs(same) - 1) s_wbase[kb * kWarps + warp] = __popc(same);
       __syncthreads();
       // (class, warp) counts in class-major order -> exclusive bases
       int2 cb_total;
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
       __syncthreads();
       s_wbase[tid] = cb.x;
       __syncthreads();
-      s_seq[s_wbase[kb * 32 + warp] + __popc(same & ((1u << lane) - 1u))] = tid;
+      s_seq[s_wbase[kb * kWarps + warp] + __popc(same & ((1u << lane) - 1u))] = tid;
     }
     __syncthreads();
     const int si = s_seq[tid];  // sequence at rank tid
@@ -231,8 +233,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
     s_doff[tid] = dec_off;  // by rank
     s_poff[tid] = pf_off;   // by sequence
     __syncthreads();
-    for (int u = tid; u < dec_total; u += kPlanThreads) {
-      const int ri = last_at_or_below(s_doff, kPlanThreads, u);
+    for (int u = tid; u < dec_total; u += kT) {
+      const int ri = last_at_or_below(s_doff, kT, u);
       const int i = s_seq[ri];
       const int ns = s_nsplit[i], r = u - s_doff[ri];
       const int h = r / ns, k = r % ns;
@@ -250,8 +252,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(rpa_params_t p, cons
       dunits[dec_base + u] = du;
       if (k == 0) counters[(int64_t)(base + i) * Hkv + h] = 0;
     }
-    for (int u = tid; u < pf_total; u += kPlanThreads) {
-      const int i = last_at_or_below(s_poff, kPlanThreads, u);
+    for (int u = tid; u < pf_total; u += kT) {
+      const int i = last_at_or_below(s_poff, kT, u);
       const int nt = s_ntiles[i], r = u - s_poff[i];
       const int h = r / nt, t = nt - 1 - r % nt;
       PrefillUnit pu;
@@ -313,7 +315,10 @@ __global__ void __launch_bounds__(256) cache_write_kernel(KvArgs a, const int32_
 // ------------------------------------------------------------ host launch
 cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int32_t* qsl,
                         const int32_t* dist, int32_t* ws, int prefill_rows, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, kv_lens, qsl, dist, ws, prefill_rows);
+  if (p.max_num_seqs <= 256)
+    plan_kernel<256><<<1, 256, 0, stream>>>(p, kv_lens, qsl, dist, ws, prefill_rows);
+  else
+    plan_kernel<1024><<<1, 1024, 0, stream>>>(p, kv_lens, qsl, dist, ws, prefill_rows);
   return cudaGetLastError();
 }
 
