@@ -204,31 +204,43 @@ def traffic_for(kernel_file: str, workload: str):
 
 
 # --------------------------------------------------------------- GPU arm
-def setup_dist(args):
+def setup_dist(backend: str = "nccl"):
+    """(world, rank, local rank) from the torchrun environment; joins the
+    process group when there is more than one rank (one GPU per rank with
+    NCCL; the host-logic tests use gloo on the CPU)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
     return world, rank, local
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
-def barrier(world):
+def barrier(world, cuda: bool = True):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if cuda:
+        torch.cuda.synchronize()
+
+
+def job_throughput(tokens_per_step: int, world: int, steps: int, seconds: float) -> float:
+    """Whole-job tokens/s: every rank runs `steps` steps of `tokens_per_step`
+    tokens (weak scaling, replicas), in `seconds` = the max over ranks."""
+    return tokens_per_step * world * steps / seconds
 
 
 def gpu_arm(args, world, rank, local):
@@ -290,7 +302,7 @@ def gpu_arm(args, world, rank, local):
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
     ms_per_step = total_s * 1e3 / args.steps
     tokens = w.num_query_tokens
-    value = tokens * world * args.steps / total_s
+    value = job_throughput(tokens, world, args.steps, total_s)
 
     # ---- end to end through the public call, host buffers, copies inside the region.
     # The step's inputs are packed into one pinned host buffer (each tensor
@@ -333,7 +345,7 @@ def gpu_arm(args, world, rank, local):
         e2e_ms.append(e0.elapsed_time(e1))
     barrier(world)
     e2e_s = max_over_ranks(sum(e2e_ms) / 1e3, world)
-    e2e_value = tokens * world * args.steps / e2e_s
+    e2e_value = job_throughput(tokens, world, args.steps, e2e_s)
 
     # ---- roofline of the dominant kernel
     peaks = load_peaks()
@@ -508,7 +520,7 @@ def main(argv=None):
             print(json.dumps(res), flush=True)
         return 0
 
-    world, rank, local = setup_dist(args)
+    world, rank, local = setup_dist()
     if world != args.gpus and rank == 0:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     res, w = gpu_arm(args, world, rank, local)
