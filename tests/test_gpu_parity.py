@@ -496,6 +496,10 @@ def test_full_decode_workload():
     _full_size("decode", sample_seqs=[0, 1, 77, 128, 255])
 
 
+def test_full_decode_d256_workload():
+    _full_size("decode_d256", sample_seqs=[0, 1, 100, 254, 255])
+
+
 def test_full_mixed_workload():
     _full_size("mixed", sample_seqs=[0, 64, 127, 128, 133, 136, 137], sample_tokens_per_seq=6)
 
