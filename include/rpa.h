@@ -41,6 +41,10 @@
  *                results never depend on it.
  *   attention_sink [Hq] fp32 or NULL.
  *   out          [T, Hq, D] bf16; rows >= qsl[S] are left untouched.
+ * Alignment: queries, keys, values, kv_cache and out start on 16 bytes (the
+ * kernels move them with bulk and tensor copies); the int32 arrays and
+ * attention_sink on 4 bytes.  A misaligned pointer is refused with
+ * RPA_ERR_INVALID_ARG before anything is enqueued.
  *
  * Semantics (per sequence s, new token i, q-head hq, kv head h = hq/(Hq/Hkv);
  * k_scale and v_scale below are those of head h when per-head scales are
@@ -74,8 +78,9 @@ extern "C" {
 
 /* Return codes of every entry point. */
 #define RPA_OK 0
-#define RPA_ERR_INVALID_ARG 1  /* null pointer, negative size, bad scale,
-                                  per-head scales with a bf16 cache        */
+#define RPA_ERR_INVALID_ARG 1  /* null or misaligned pointer, negative size,
+                                  bad scale, per-head scales with a bf16
+                                  cache                                    */
 #define RPA_ERR_UNSUPPORTED 2  /* head_dim not 64/96/128/192/256, Hq/Hkv not in {1,2,4,8,16},
                                   page_size not a power of two in [1,1024],
                                   or an fp8 cache with head_dim 64/96 and

@@ -133,7 +133,8 @@ def forward(queries, keys, values, kv_cache, kv_lens, block_tables, query_start_
         _need(t, name, (torch.int32,), dev)
     if attention_sink is not None:
         _need(attention_sink, "attention_sink", (torch.float32,), dev)
-    if queries.dim() != 3 or keys.shape != values.shape or keys.shape[0] != queries.shape[0]:
+    if (queries.dim() != 3 or keys.dim() != 3 or keys.shape != values.shape or
+            keys.shape[0] != queries.shape[0] or keys.shape[2] != queries.shape[2]):
         raise ValueError("queries [T,Hq,D], keys/values [T,Hkv,D] expected")
     if query_start_loc.numel() != kv_lens.numel() + 1 or distribution.numel() != 3:
         raise ValueError("query_start_loc must have max_num_seqs+1 entries, distribution 3")

@@ -102,6 +102,9 @@ static int forward_impl(const rpa_params_t* params, const void* queries, const v
   if (!queries || !keys || !values || !kv_cache || !kv_lens || !block_tables ||
       !query_start_loc || !distribution || !out)
     return RPA_ERR_INVALID_ARG;
+  if (!pointers_aligned(queries, keys, values, kv_cache, out, kv_lens, block_tables,
+                        query_start_loc, distribution, attention_sink))
+    return RPA_ERR_INVALID_ARG;
   rc = check_ws(params, workspace, workspace_bytes);
   if (rc) return rc;
   const int sms = num_sms_current();
@@ -136,6 +139,9 @@ int rpa_update_cache(const rpa_params_t* params, const void* keys, const void* v
   if (rc) return rc;
   if (!keys || !values || !kv_cache || !kv_lens || !block_tables || !query_start_loc ||
       !distribution)
+    return RPA_ERR_INVALID_ARG;
+  if (!pointers_aligned(nullptr, keys, values, kv_cache, nullptr, kv_lens, block_tables,
+                        query_start_loc, distribution, nullptr))
     return RPA_ERR_INVALID_ARG;
   rc = check_ws(params, workspace, workspace_bytes);
   if (rc) return rc;

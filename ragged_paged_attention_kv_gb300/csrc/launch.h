@@ -19,6 +19,19 @@ cudaError_t launch_prefill(const AttnArgs& a, int max_units, int num_sms, cudaSt
 bool prefill_uses_tc(const rpa_params_t& p);
 cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
 
+// The alignment the kernels' bulk and tensor copies rely on: the bf16
+// tensors and the cache on 16 bytes, the int32 arrays and the sink on 4.
+// Null pointers pass (each entry point checks the ones it requires).
+inline bool pointers_aligned(const void* queries, const void* keys, const void* values,
+                             const void* kv_cache, const void* out, const void* kv_lens,
+                             const void* block_tables, const void* query_start_loc,
+                             const void* distribution, const void* attention_sink) {
+  auto on = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
+  return on(queries, 16) && on(keys, 16) && on(values, 16) && on(kv_cache, 16) && on(out, 16) &&
+         on(kv_lens, 4) && on(block_tables, 4) && on(query_start_loc, 4) && on(distribution, 4) &&
+         on(attention_sink, 4);
+}
+
 // Rows of a prefill tile for these params (the planner and the kernels agree on it).
 inline int prefill_rows_for(const rpa_params_t& p) { return prefill_uses_tc(p) ? 256 : kPrefillRows; }
 

@@ -63,6 +63,9 @@ extern "C" int rpa_forward_noalloc(const rpa_params_t* params, const void* queri
   if (!queries || !keys || !values || !kv_cache || !kv_lens || !block_tables ||
       !query_start_loc || !distribution || !out)
     return RPA_ERR_INVALID_ARG;
+  if (!pointers_aligned(queries, keys, values, kv_cache, out, kv_lens, block_tables,
+                        query_start_loc, distribution, attention_sink))
+    return RPA_ERR_INVALID_ARG;
   void* ws = nullptr;
   if (static_workspace(&ws) != cudaSuccess) return RPA_ERR_CUDA;
   int dev = 0, sms = 0;

@@ -129,3 +129,40 @@ def test_binding_raises_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         _lib.load()
+
+
+@pytest.mark.parametrize("which", ["queries", "keys", "values", "kv_cache", "out", "kv_lens",
+                                   "block_tables", "query_start_loc", "distribution", "sink"])
+def test_misaligned_pointers_are_refused_before_any_gpu_work(lib, which):
+    """Valid params with one misaligned pointer: refused on the host
+    (checked before the workspace and before any CUDA call)."""
+    p = _params()
+    ptrs = {k: ctypes.c_void_p(1 << 20) for k in ("queries", "keys", "values", "kv_cache", "out",
+                                                  "kv_lens", "block_tables", "query_start_loc",
+                                                  "distribution", "sink")}
+    ptrs[which] = ctypes.c_void_p((1 << 20) + (8 if which in ("queries", "keys", "values",
+                                                              "kv_cache", "out") else 2))
+    ws = ctypes.c_void_p(1 << 21)
+    rc = lib.rpa_forward(ctypes.byref(p), ptrs["queries"], ptrs["keys"], ptrs["values"],
+                         ptrs["kv_cache"], ptrs["kv_lens"], ptrs["block_tables"],
+                         ptrs["query_start_loc"], ptrs["distribution"], ptrs["sink"],
+                         ptrs["out"], ws, 1 << 40, None)
+    assert rc == 1
+    if which in ("keys", "values", "kv_cache", "kv_lens", "block_tables", "query_start_loc",
+                 "distribution"):
+        rc = lib.rpa_update_cache(ctypes.byref(p), ptrs["keys"], ptrs["values"], ptrs["kv_cache"],
+                                  ptrs["kv_lens"], ptrs["block_tables"], ptrs["query_start_loc"],
+                                  ptrs["distribution"], ws, 1 << 40, None)
+        assert rc == 1
+
+
+def test_binding_rejects_mismatched_head_dims():
+    import torch
+    import ragged_paged_attention_kv_gb300 as rpa
+    T, S = 4, 2
+    q = torch.zeros(T, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(T, 2, 32, dtype=torch.bfloat16)
+    cache = torch.zeros(4, 16, 4, 32, dtype=torch.bfloat16)
+    i32 = lambda n: torch.zeros(n, dtype=torch.int32)  # noqa: E731
+    with pytest.raises(ValueError):
+        rpa.forward(q, k, k.clone(), cache, i32(S), i32(S * 4), i32(S + 1), i32(3))
