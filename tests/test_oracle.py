@@ -385,3 +385,49 @@ def test_equal_per_head_scales_are_the_scalar_scales():
     shape = (base.num_pages * base.page_size, 2 * base.num_kv_heads, base.head_dim)
     d = (c0 != c2).reshape(shape).any(axis=(0, 2))
     assert d[4] and d[5] and not d[[0, 1, 2, 3, 6, 7]].any()
+
+
+# ------------------------------------------------------------ random sweep
+def _random_case(i):
+    """A seeded random small call: shapes, ragged lengths (some q_len = 0),
+    every option on or off, fp8 with scalar or per-head scales."""
+    rng = np.random.default_rng(1000 + i)
+    Hkv = int(rng.integers(1, 4))
+    G = int(rng.choice([1, 2, 4]))
+    D = int(rng.choice([8, 16, 24]))
+    P = int(rng.choice([1, 2, 4, 8]))
+    S = int(rng.integers(1, 5))
+    q_lens = [int(x) for x in rng.integers(0, 7, size=S)]
+    kv_lens = [q + int(rng.integers(0, 21)) for q in q_lens]
+    kv_lens = [max(kv, 1) for kv in kv_lens]
+    kw = dict(num_q_heads=Hkv * G, num_kv_heads=Hkv, head_dim=D, page_size=P,
+              softmax_scale=float(rng.uniform(0.2, 1.2)),
+              sliding_window=int(rng.choice([0, 0, 1, 3, 7])),
+              logits_soft_cap=float(rng.choice([0.0, 0.0, 2.5, 20.0])),
+              has_sink=bool(rng.integers(0, 2)))
+    if rng.integers(0, 2):
+        kw["kv_dtype"] = "fp8"
+        if rng.integers(0, 2):
+            kw["k_scale_heads"] = [float(x) for x in rng.uniform(0.01, 0.3, Hkv)]
+            kw["v_scale_heads"] = [float(x) for x in rng.uniform(0.01, 0.3, Hkv)]
+        else:
+            kw["k_scale"], kw["v_scale"] = float(rng.uniform(0.02, 0.2)), float(rng.uniform(0.02, 0.2))
+    # decode class: a prefix of the one-token sequences
+    d0 = 0
+    while d0 < S and q_lens[d0] == 1:
+        d0 += 1
+    d0 = int(rng.integers(0, d0 + 1))
+    d1 = int(rng.integers(d0, S + 1))
+    kw["distribution"] = [d0, d1, S]
+    return wl.make_custom(f"r{i}", 2000 + i, q_lens, kv_lens, **kw)
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_oracle_matches_dense_brute_force_random(i):
+    w = _random_case(i)
+    q, k, v, pool, sink = _inputs(w)
+    out, cache = run_oracle(w, q, k, v, pool, sink)
+    ref = dense_attention(w, q, k, v, pool, sink)
+    assert out.shape == ref.shape
+    assert np.max(np.abs(out - ref), initial=0.0) < 1e-10
+    assert np.array_equal(cache, pool_bytes(expected_pool_after(w, pool, k, v)))
