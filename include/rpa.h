@@ -178,23 +178,31 @@ int rpa_forward_timed(const rpa_params_t* params, const void* queries,
  *
  * Instead of a caller workspace it uses one fixed array of
  * RPA_NOALLOC_WORKSPACE_BYTES in device global memory, reserved when the
- * library is loaded and held by every GPU that loads it until the process
- * exits.  The caller still passes all inputs and outputs, exactly as for
+ * library's device code is loaded into a context and held there until the
+ * context is destroyed (for the primary context of a device: process exit
+ * or cudaDeviceReset), so every GPU that uses the library holds it.  The caller still passes all inputs and outputs, exactly as for
  * rpa_forward, and gets the same results.  The call allocates nothing and
  * calls no allocating routine.
  *
  * - Params whose workspace (rpa_workspace_size) exceeds the array are
  *   refused with RPA_ERR_NOALLOC_TOO_LARGE; nothing is enqueued.
- * - The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.  Later calls reuse the address.
- * - Every call on a device shares the one array and leaves its contents
+ * - Every call looks up the array's device address in the current context
+ *   (cudaGetSymbolAddress; each context has its own copy of the array, so
+ *   the address is never cached).  The first call in a context may load the
+ *   library's device code into it; make that first call before any stream
+ *   capture.  Once loaded, the lookup allocates nothing.
+ * - Every call in a context shares the one array and leaves its contents
  *   behind; the planner rewrites every word the kernels read, so nothing has
  *   to be cleared between calls.  Calls whose GPU work overlaps (on
  *   different streams, or different host threads without ordering) race on
  *   the array and give undefined results: serialise them.
- * - The device status word of these calls is not readable through
- *   rpa_get_status (there is no caller workspace to pass). */
+ * - The device status word of these calls is not readable (there is no
+ *   caller workspace to pass to rpa_get_status).  The problems it reports
+ *   -- page ids outside the pool, inconsistent kv_lens / query_start_loc /
+ *   distribution, bad per-head scales, a bounded device wait that gave up --
+ *   therefore go unreported: callers of this entry point must check their
+ *   metadata themselves, and a sequence the kernels skip keeps whatever its
+ *   output rows held. */
 #define RPA_NOALLOC_WORKSPACE_BYTES (32u << 20)
 #define RPA_ERR_NOALLOC_TOO_LARGE 5
 int rpa_forward_noalloc(const rpa_params_t* params, const void* queries,
@@ -208,7 +216,7 @@ int rpa_forward_noalloc(const rpa_params_t* params, const void* queries,
  * to *device_status (a host int32) and synchronises the stream.  0 = clean. */
 int rpa_get_status(const void* workspace, void* stream, int32_t* device_status);
 
-/* Static text for a return code (RPA_OK ... RPA_ERR_CUDA). */
+/* Static text for a return code (RPA_OK ... RPA_ERR_NOALLOC_TOO_LARGE). */
 const char* rpa_status_string(int code);
 
 #ifdef __cplusplus

@@ -17,6 +17,7 @@ RPA_ERR_INVALID_ARG = 1
 RPA_ERR_UNSUPPORTED = 2
 RPA_ERR_WORKSPACE = 3
 RPA_ERR_CUDA = 4
+RPA_ERR_NOALLOC_TOO_LARGE = 5
 
 RPA_STATUS_BAD_PAGE = 0x1
 RPA_STATUS_BAD_KV_LEN = 0x2
@@ -31,7 +32,7 @@ RPA_KV_FP8_E4M3 = 1
 
 # Every symbol include/rpa.h declares.
 EXPORTS = ("rpa_workspace_size", "rpa_update_cache", "rpa_forward", "rpa_forward_timed",
-           "rpa_get_status", "rpa_status_string")
+           "rpa_forward_noalloc", "rpa_get_status", "rpa_status_string")
 
 
 class RpaParams(ctypes.Structure):
@@ -88,6 +89,8 @@ def load() -> ctypes.CDLL:
         lib.rpa_forward_timed.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                           ctypes.c_size_t, vp, ctypes.POINTER(ctypes.c_void_p)]
         lib.rpa_forward_timed.restype = ctypes.c_int
+        lib.rpa_forward_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.rpa_forward_noalloc.restype = ctypes.c_int
         lib.rpa_get_status.argtypes = [vp, vp, i32p]
         lib.rpa_get_status.restype = ctypes.c_int
         lib.rpa_status_string.argtypes = [ctypes.c_int]

@@ -7,11 +7,11 @@
 // allocation and expose none to extensions, or setups that forbid any
 // allocation after start-up.  For them this entry point takes its scratch
 // memory (the planner's work lists, the split-KV partial results and their
-// counters) from one fixed array in device global memory, reserved when the
-// library is loaded and held by every GPU that loads it until the process
-// exits.  It allocates nothing itself and calls no allocating routine.
-#include <mutex>
-
+// counters) from one fixed array in device global memory.  The array is
+// reserved when the library's device code is loaded into a context and held
+// there until that context is destroyed (for the primary context: process
+// exit or cudaDeviceReset).  The entry point allocates nothing itself and
+// calls no allocating routine.
 #include "common.cuh"
 #include "kv_write.cuh"
 
@@ -25,26 +25,14 @@ namespace rpa {
 static __device__ __align__(256) uint8_t g_static_workspace[RPA_NOALLOC_WORKSPACE_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_ws_addr[kMaxDevices] = {};  // device address of the array, per device
-
-// Resolves the array's device address on the current device (once per
-// device; later calls reuse it).
+// The array's device address in the current context.  It is looked up on
+// every call rather than cached: each context holds its own copy of the
+// array (a context made with cuCtxCreate next to the primary one, or the
+// primary context rebuilt after cudaDeviceReset, puts it at another
+// address).  Once the library's module is loaded in the context, the lookup
+// allocates nothing.
 cudaError_t static_workspace(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ws_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_workspace);
-    if (e != cudaSuccess) return e;
-    g_ws_addr[dev] = p;
-  }
-  *out = g_ws_addr[dev];
-  return cudaSuccess;
+  return cudaGetSymbolAddress(out, g_static_workspace);
 }
 }  // namespace
 }  // namespace rpa

@@ -105,6 +105,8 @@ struct UnitGeom {
   int seq, h, q0, q_len, kv_len, ctx, t_begin, t_end;
   int lo;              // first key any row of the tile may see
   int c_start, n_cached, i0, n_tiles;
+  // rows of a tile starting at key0 that lie before every row's window
+  __device__ int lead(int key0) const { return lo > key0 ? lo - key0 : 0; }
   __device__ void tile(int j, bool& is_new, int& key0, int& valid) const {
     if (j < n_cached) {
       is_new = false;
@@ -219,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warps (part 0..kDecWarps-1).  Cached rows are decoded from their e4m3
   // codes; new rows, which came as bf16 from the inputs, are quantised and
   // decoded in place so they carry exactly the codes the page write stores.
-  // Value rows past the valid range become zero; key rows there are masked
-  // by the softmax.
+  // Value rows no row of the unit may see (past the valid range, or before
+  // the window) become zero; key rows there are masked by the softmax.
   auto staging = [&](uint32_t tc, int kv) -> uint32_t {
     return C::kOffStg + (2 * (C::kStgPerOp == 2 ? (tc & 1) : 0) + kv) * C::kStaging;
   };
@@ -233,10 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale = !PH ? (kv ? p.v_scale : p.k_scale)
                             : (kv ? v_scale_of(p, g.h) : k_scale_of(p, g.h));
     const int rows = kv ? kN : valid;
+    const int lead = kv ? g.lead(key0) : 0;
     for (int idx = 32 * part + lane; idx < rows * (D / 8); idx += 32 * kDecWarps) {
       const int r = idx / (D / 8), c = idx % (D / 8);
       uint4* dst = reinterpret_cast<uint4*>(op + (c >> 3) * kHalf + sw128(r, c & 7));
-      if (r >= valid) {
+      if (r >= valid || r < lead) {
         *dst = make_uint4(0, 0, 0, 0);
       } else if (is_new) {
         *dst = dequant8(quantize8(*dst, scale));
@@ -352,10 +355,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool is_new;
           int key0, valid;
           g.tile(j, is_new, key0, valid);
-          if (valid < kN) {
+          const int lead = g.lead(key0);
+          if (valid < kN || lead > 0) {
+            // zero the value rows [0, lead) and [valid, kN): their keys are
+            // masked, but their bytes may be anything (0 * NaN poisons P V)
             uint8_t* v = smem + kOffV + s * kOperand;
-            for (int idx = lane; idx < (kN - valid) * 8 * C::kHalves; idx += 32) {
-              const int r = valid + idx / (8 * C::kHalves), c = idx % (8 * C::kHalves);
+            constexpr int kRowChunks = 8 * C::kHalves;
+            const int tail = kN - valid;
+            for (int idx = lane; idx < (lead + tail) * kRowChunks; idx += 32) {
+              const int i = idx / kRowChunks, c = idx % kRowChunks;
+              const int r = i < lead ? i : valid + (i - lead);
               *reinterpret_cast<uint4*>(v + (c >> 3) * kHalf + r * 128 + (c & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }

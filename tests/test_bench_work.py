@@ -16,7 +16,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
-from ragged_paged_attention_kv_gb300 import workloads as wl  # noqa: E402
+import workloads as wl  # noqa: E402
 
 
 def _one(q_len, kv_len, *, decode, **kw):

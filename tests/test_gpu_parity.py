@@ -17,8 +17,8 @@ import torch
 
 import oracle
 import ragged_paged_attention_kv_gb300 as rpa
-from helpers import assert_close, bf16_half_ulp, pool_bytes, run_oracle
-from ragged_paged_attention_kv_gb300 import workloads as wl
+from helpers import assert_close, bf16_half_ulp, poison_unread_slots, pool_bytes, run_oracle
+import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
@@ -58,9 +58,12 @@ def run_gpu(w, q, k, v, pool_before, sink=None, workspace=None, out=None):
     return out_t.float().cpu().numpy().astype(np.float64), pool.cpu(), status
 
 
-def check_case(w, expect_status=0):
+def check_case(w, expect_status=0, poison=False):
+    """poison: the slots no query may read hold NaN / Inf bit patterns."""
     q, k, v = w.make_qkv()
     pool = w.make_pool("cpu")
+    if poison:
+        pool = poison_unread_slots(w, pool)
     sink = w.make_sink()
     ref_out, ref_cache = run_oracle(w, q, k, v, pool, sink)
     out, pool_after, status = run_gpu(w, q, k, v, pool, sink)
@@ -207,6 +210,55 @@ TC_CASES = [
 @pytest.mark.parametrize("name,make", TC_CASES, ids=[c[0] for c in TC_CASES])
 def test_tcgen05_prefill_cases(name, make):
     check_case(make())
+
+
+# Slots that no query may read -- rows past kv_len in a sequence's last page,
+# rows before the window, the new tokens' slots before they are written,
+# unused pages -- hold NaN / Inf bit patterns (bf16 0x7FC0, 0x7F80, 0xFF80,
+# 0xFFC1; e4m3 0x7F, 0xFF).  A serving pool holds arbitrary bytes there (the
+# ejkernel ragged_page_attention_v3 docstring: only the first num_seqs
+# entries of kv_lens / block_tables are valid).  The outputs must stay finite
+# and within tolerance and the pool bit-exact, on every kernel path: the
+# decode kernel, the tcgen05 prefill (bf16 and fp8 staging) and the
+# warp-level MMA prefill (pages of 4 rows; head_dim 256).
+POISON_CASES = [
+    ("decode_window_splits", lambda: _case("z1", 301, [1] * 6, [700, 17, 1290, 333, 65, 1],
+                                           num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                           sliding_window=100)),
+    ("decode_partial_pages", lambda: _case("z2", 302, [1] * 5, [700, 17, 1290, 333, 65],
+                                           num_q_heads=32, num_kv_heads=8, head_dim=128)),
+    ("decode_fp8_window_options", lambda: _case("z3", 303, [1] * 5, [900, 129, 5, 2000, 77],
+                                                kv_dtype="fp8", k_scale=0.05, v_scale=0.07,
+                                                num_q_heads=64, num_kv_heads=8,
+                                                logits_soft_cap=30.0, has_sink=True,
+                                                sliding_window=128)),
+    ("decode_d256_window", lambda: _case("z4", 304, [1] * 4, [300, 5, 1300, 90], num_q_heads=16,
+                                         num_kv_heads=8, head_dim=256, sliding_window=64)),
+    ("tc_prefill_window_cached", lambda: _tc("z5", 305, [1, 100, 64, 200], [2000, 1500, 64, 700],
+                                             sliding_window=200)),
+    ("tc_prefill_partial_pages", lambda: _tc("z6", 306, [130, 1, 7], [1000, 70, 135],
+                                             page_size=64)),
+    ("tc_prefill_p256_window", lambda: _tc("z7", 307, [150, 40], [1000, 40], page_size=256,
+                                           sliding_window=300)),
+    ("tc_prefill_fp8_options", lambda: _case("z8", 308, [1, 1, 64, 20], [900, 129, 200, 20],
+                                             kv_dtype="fp8", k_scale=0.05, v_scale=0.07,
+                                             num_q_heads=64, num_kv_heads=8,
+                                             logits_soft_cap=30.0, has_sink=True,
+                                             sliding_window=128)),
+    ("tc_prefill_fp8_d128_window", lambda: _case("z9", 309, [1, 90, 33], [600, 500, 33],
+                                                 kv_dtype="fp8", k_scale=0.3, v_scale=0.1,
+                                                 head_dim=128, sliding_window=77)),
+    ("mma_prefill_p4_window", lambda: _case("z10", 310, [1, 25, 9], [90, 60, 40], page_size=4,
+                                            sliding_window=20)),
+    ("mma_prefill_d256_fp8_window", lambda: _case("z11", 311, [1, 70, 8], [900, 200, 8],
+                                                  kv_dtype="fp8", head_dim=256, k_scale=0.05,
+                                                  v_scale=0.07, sliding_window=50)),
+]
+
+
+@pytest.mark.parametrize("name,make", POISON_CASES, ids=[c[0] for c in POISON_CASES])
+def test_nonfinite_bytes_in_unread_slots(name, make):
+    check_case(make(), poison=True)
 
 
 def test_decode_split_boundaries():
@@ -420,11 +472,42 @@ def test_fp8_quantisation_sweep_matches_oracle():
 
 
 # ------------------------------------------------------- full-size workloads
-def _full_size(name, sample_seqs, sample_tokens_per_seq=None, nthreads=0):
+def _check_subset(w, seqs, pool0, pool, out, q, k, v, sink, sample_tokens_per_seq, nthreads):
+    """The listed sequences of a full-size call against the oracle: their
+    pages after the call bit for bit, and their outputs (every new token, or
+    the first, middle, last and a seeded sample of them)."""
+    sub, sub_pool, tmap = w.subset(seqs, pool0)
+    p = oracle.make_params(**sub.params())
+    cache = oracle.update_cache(p, k[tmap], v[tmap], pool_bytes(sub_pool), sub.kv_lens,
+                                sub.block_tables, sub.query_start_loc, sub.num_seqs)
+    pages = np.concatenate([w.pages_of(s) for s in seqs]).astype(np.int64)
+    got_pages = pool.index_select(0, torch.as_tensor(pages, device=DEV)).cpu()
+    assert np.array_equal(pool_bytes(got_pages), cache[:len(pages) * (cache.size // sub.num_pages)])
+    if sample_tokens_per_seq is None:
+        rows = np.arange(len(tmap))
+    else:
+        rng = np.random.default_rng(5)
+        sqsl = sub.query_start_loc
+        rows = []
+        for i in range(sub.num_seqs):
+            a_, b_ = int(sqsl[i]), int(sqsl[i + 1])
+            pick = {a_, b_ - 1, a_ + (b_ - a_) // 2}
+            pick |= set(rng.integers(a_, b_, size=sample_tokens_per_seq).tolist())
+            rows += sorted(pick)
+        rows = np.array(rows)
+    ref = oracle.attention_rows(p, q[tmap], cache, sub.kv_lens, sub.block_tables,
+                                sub.query_start_loc, sub.num_seqs, rows,
+                                None if sink is None else sink.numpy(), nthreads)
+    got = out[torch.as_tensor(tmap[rows], device=DEV)].float().cpu().numpy().astype(np.float64)
+    return got, ref
+
+
+def _full_size(name, prefill_seqs=(), sample_tokens_per_seq=None, nthreads=0, batch=32):
     """rpa_forward on the full workload, in the benchmark's launch
-    configuration; sampled sequences are checked against the oracle (outputs
-    and their pages) and the whole pool outside the new-token slots must be
-    unchanged."""
+    configuration.  Every new-token slot (and nothing else) of the pool must
+    change as the page write says; EVERY decode-class sequence is checked
+    against the oracle (outputs and pages, in batches of `batch` sequences),
+    and the listed prefill sequences on sampled tokens."""
     w = wl.get(name)
     q, k, v = w.make_qkv()
     sink = w.make_sink()
@@ -443,7 +526,6 @@ def _full_size(name, sample_seqs, sample_tokens_per_seq=None, nthreads=0):
     assert rpa.get_status(ws) == 0
     torch.cuda.synchronize()
     # every new token's slot, and nothing else, changed as the page write says
-    qsl = w.query_start_loc
     flat0 = pool0.view(w.num_pages * w.page_size, 2 * w.num_kv_heads, w.head_dim)
     flat1 = pool.view(w.num_pages * w.page_size, 2 * w.num_kv_heads, w.head_dim)
     slots = []
@@ -463,51 +545,42 @@ def _full_size(name, sample_seqs, sample_tokens_per_seq=None, nthreads=0):
     nq = w.num_query_tokens
     assert torch.equal(flat1[slots][:, 0::2], kd[:nq]) and torch.equal(flat1[slots][:, 1::2], vd[:nq])
     assert torch.all(out[nq:] == 7.0)
-    # sampled sequences against the oracle
-    sub, sub_pool, tmap = w.subset(sample_seqs, pool0)
-    p = oracle.make_params(**sub.params())
-    cache = oracle.update_cache(p, k[tmap], v[tmap], pool_bytes(sub_pool), sub.kv_lens,
-                                sub.block_tables, sub.query_start_loc, sub.num_seqs)
-    # the sampled pages after the call, bit for bit
-    pages = np.concatenate([w.pages_of(s) for s in sample_seqs]).astype(np.int64)
-    got_pages = pool.index_select(0, torch.as_tensor(pages, device=DEV)).cpu()
-    n_used = len(pages)
-    assert np.array_equal(pool_bytes(got_pages), cache[:n_used * (cache.size // sub.num_pages)])
-    if sample_tokens_per_seq is None:
-        rows = np.arange(len(tmap))
-    else:
-        rng = np.random.default_rng(5)
-        sqsl = sub.query_start_loc
-        rows = []
-        for i in range(sub.num_seqs):
-            a_, b_ = int(sqsl[i]), int(sqsl[i + 1])
-            pick = {a_, b_ - 1, a_ + (b_ - a_) // 2}
-            pick |= set(rng.integers(a_, b_, size=sample_tokens_per_seq).tolist())
-            rows += sorted(pick)
-        rows = np.array(rows)
-    ref = oracle.attention_rows(p, q[tmap], cache, sub.kv_lens, sub.block_tables,
-                                sub.query_start_loc, sub.num_seqs, rows,
-                                None if sink is None else sink.numpy(), nthreads)
-    got = out[torch.as_tensor(tmap[rows], device=DEV)].float().cpu().numpy().astype(np.float64)
-    assert_close(got, ref, name)
+    del flat0, flat1, changed, kd, vd
+    decode_seqs = [s for s in range(w.num_seqs)
+                   if s < int(w.distribution[0]) and int(w.q_lens[s]) == 1]
+    gots, refs = [], []
+    for i in range(0, len(decode_seqs), batch):
+        g_, r_ = _check_subset(w, decode_seqs[i:i + batch], pool0, pool, out, q, k, v, sink,
+                               None, nthreads)
+        gots.append(g_)
+        refs.append(r_)
+    if prefill_seqs:
+        g_, r_ = _check_subset(w, list(prefill_seqs), pool0, pool, out, q, k, v, sink,
+                               sample_tokens_per_seq, nthreads)
+        gots.append(g_)
+        refs.append(r_)
+    assert_close(np.concatenate(gots), np.concatenate(refs), name)
+    return len(decode_seqs)
 
 
 def test_full_decode_workload():
-    _full_size("decode", sample_seqs=[0, 1, 77, 128, 255])
+    assert _full_size("decode") == 256
 
 
 def test_full_decode_d256_workload():
-    _full_size("decode_d256", sample_seqs=[0, 1, 100, 254, 255])
+    assert _full_size("decode_d256") == 256
 
 
 def test_full_mixed_workload():
-    _full_size("mixed", sample_seqs=[0, 64, 127, 128, 133, 136, 137], sample_tokens_per_seq=6)
+    assert _full_size("mixed", prefill_seqs=[128, 131, 133, 135, 136, 137],
+                      sample_tokens_per_seq=6) == 128
 
 
 def test_full_fp8_workload():
-    _full_size("fp8", sample_seqs=[0, 100, 511, 512, 519], sample_tokens_per_seq=8)
+    assert _full_size("fp8", prefill_seqs=[512, 515, 519], sample_tokens_per_seq=8,
+                      batch=64) == 512
 
 
 @pytest.mark.parametrize("name", ["long", "long_w4096"])
 def test_full_long_workload(name):
-    _full_size(name, sample_seqs=[0, 1], sample_tokens_per_seq=6)
+    _full_size(name, prefill_seqs=[0, 1], sample_tokens_per_seq=6)

@@ -17,7 +17,7 @@ import torch
 import oracle
 from dense_reference import dense_attention, expected_pool_after, fp8_roundtrip
 from helpers import pool_bytes, run_oracle
-from ragged_paged_attention_kv_gb300 import workloads as wl
+import workloads as wl
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -431,3 +431,66 @@ def test_oracle_matches_dense_brute_force_random(i):
     assert out.shape == ref.shape
     assert np.max(np.abs(out - ref), initial=0.0) < 1e-10
     assert np.array_equal(cache, pool_bytes(expected_pool_after(w, pool, k, v)))
+
+
+# ------------------------------------------------- unread slots, tolerance
+@pytest.mark.parametrize("kind", ["bf16_window", "bf16", "fp8_window_options"])
+def test_oracle_reads_no_slot_outside_the_band(kind):
+    """Slots outside [window start, ctx) of every sequence -- rows past
+    kv_len, rows before the window, the new tokens' slots before the write,
+    unused pages -- filled with NaN / Inf change nothing: the outputs equal
+    those on the clean pool bit for bit and the poisoned bytes pass through
+    the page write untouched.  This also checks the GPU tests' read_slots."""
+    from helpers import poison_unread_slots, read_slots
+    extra = {"bf16_window": dict(sliding_window=37),
+             "bf16": {},
+             "fp8_window_options": dict(kv_dtype="fp8", k_scale=0.05, v_scale=0.07,
+                                        logits_soft_cap=30.0, has_sink=True,
+                                        sliding_window=20)}[kind]
+    w = wl.make_custom("poison", 77, [1, 1, 40, 9, 0], [300, 5, 140, 9, 12], num_q_heads=8,
+                       num_kv_heads=2, head_dim=64, page_size=16, **extra)
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu")
+    sink = w.make_sink()
+    bad = poison_unread_slots(w, pool)
+    out_clean, cache_clean = run_oracle(w, q, k, v, pool, sink)
+    out_bad, cache_bad = run_oracle(w, q, k, v, bad, sink)
+    assert np.all(np.isfinite(out_bad))
+    assert np.array_equal(out_bad, out_clean)
+    # every slot is either read (identical bytes) or carries its poison,
+    # except the new tokens' slots, which both writes fill identically
+    rows = w.num_pages * w.page_size
+    cb = cache_bad.reshape(rows, -1)
+    cc = cache_clean.reshape(rows, -1)
+    written = np.zeros(rows, bool)
+    for s in range(w.num_seqs):
+        ctx = int(w.kv_lens_valid[s]) - int(w.q_lens[s])
+        pos = np.arange(ctx, int(w.kv_lens_valid[s]))
+        written[w.block_tables[s * w.pages_per_seq + pos // w.page_size] * w.page_size
+                + pos % w.page_size] = True
+    assert np.array_equal(cb[written | read_slots(w)], cc[written | read_slots(w)])
+    assert np.array_equal(cb[~(written | read_slots(w))],
+                          pool_bytes(bad).reshape(rows, -1)[~(written | read_slots(w))])
+
+
+def test_tolerance_rule_is_the_stated_bound_where_attainable():
+    """max |err| <= 1e-2 wherever |exact| < 4 (the correctly rounded bf16
+    output is always within half an ulp <= 2^-7 there); from |exact| = 4 on,
+    the bound adds the output's own rounding, half an ulp >= 2^-6."""
+    from helpers import assert_close, max_abs_bound, output_errors
+    exact = np.array([0.0, 0.3, 1.5, 3.99, 4.0, 7.9, 8.0, 100.0])
+    b = max_abs_bound(exact)
+    assert np.all(b[:4] == 1e-2)
+    assert b[4] == 2.0 ** -6 + 1e-2 and b[5] == 2.0 ** -6 + 1e-2
+    assert b[6] == 2.0 ** -5 + 1e-2 and b[7] == 2.0 ** -2 + 1e-2
+    # the correctly rounded bf16 value always meets the max rule, at any
+    # magnitude (the mean rule is a property of the data, checked separately)
+    x = np.random.default_rng(0).normal(0, 30, 20000)
+    rounded = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    assert output_errors(rounded, x)[0] <= 1.0
+    # an error of 0.011 at |exact| = 2 (where half an ulp is 2^-8) fails
+    y = np.full(1000, 2.0)
+    y_got = y.copy()
+    y_got[0] += 0.011
+    with pytest.raises(AssertionError):
+        assert_close(y_got, y, "one element off by 0.011")

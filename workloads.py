@@ -29,6 +29,9 @@ from ``torch.Generator().manual_seed(1000 + k)`` on the CPU):
   fp8      512 decode (kv ~ U[256,16384]) + 8 chunks of 256 (prior kv ~
            U[0,8192]); Hq64/Hkv8/D64/P16; fp8 e4m3 cache, k/v scale 0.05,
            soft cap 30, sinks ~ N(0,1), sliding_window 128, scale 1/8.
+  decode_d256, long_d256
+           head_dim 256 (Gemma-2-9B attention shape): 256 decode seqs with
+           window 4096 and cap 50; 2 x 8192 causal prefill.
 """
 from __future__ import annotations
 
@@ -394,6 +397,27 @@ def long(sliding_window: int = 0) -> Workload:
                     distribution=np.array([0, 0, 2], np.int32), total_tokens=2 * L)
 
 
+def long_d256() -> Workload:
+    """Long causal prefill at head_dim 256 (Gemma-2-9B attention shape
+    without its window and cap): 2 seqs q = kv = 8192, Hq16/Hkv8/D256, bf16
+    cache, page_size 64, scale 1/16."""
+    seed = 1016
+    g = torch.Generator().manual_seed(seed)
+    P, L = 64, 8192
+    q = np.full(2, L, np.int32)
+    kv = np.full(2, L, np.int32)
+    pps = L // P
+    need = 2 * pps
+    num_pages = int(need * 1.1) + 1
+    bt = _assign_pages(kv, P, num_pages, 2, pps, g)
+    return Workload(name="long_d256", seed=seed, num_q_heads=16, num_kv_heads=8, head_dim=256,
+                    page_size=P, num_pages=num_pages, pages_per_seq=pps, max_num_seqs=2,
+                    kv_dtype="bf16", softmax_scale=1.0 / 16.0, sliding_window=0,
+                    logits_soft_cap=0.0, k_scale=1.0, v_scale=1.0, has_sink=False,
+                    q_lens=q, kv_lens_valid=kv, block_tables=bt,
+                    distribution=np.array([0, 0, 2], np.int32), total_tokens=2 * L)
+
+
 def long_small() -> Workload:
     """The long-context shape at one sequence of 8192 tokens (profiling size)."""
     seed = 1014
@@ -466,6 +490,7 @@ WORKLOADS = {
     "fp8_small": fp8_small,
     "decode_d256": decode_d256,
     "decode_d256_small": lambda: decode_d256(64, "decode_d256_small"),
+    "long_d256": long_d256,
 }
 
 
