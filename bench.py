@@ -8,8 +8,10 @@ One step = one rpa_forward over one synthetic batch (planner, decode kernel,
 prefill kernel; the page write is fused into the two attention kernels).
 Inputs are resident in HBM when the timed region starts; L2 is flushed (a 512 MB
 write) before every timed step, outside its events.  Each step is timed
-with CUDA events on the launching stream, and each kernel inside it with the
-events rpa_forward_timed records.  With N > 1 (torchrun) every rank runs an
+with two CUDA events on the launching stream (the attention kernels are
+programmatic dependents of the kernel before them, so no event sits between
+them); each kernel's own time comes from a second set of steps run through
+rpa_forward_timed, whose events sit between the kernels.  With N > 1 (torchrun) every rank runs an
 independent replica ("replicas only": the op has no exchange step), the time
 is the max over ranks, and value counts the tokens of all ranks.
 
@@ -327,33 +329,49 @@ def step(ctx, events=None, src=None):
 
 
 def time_steps(ctx, steps, warmup, flush, stream, world, rank, dev):
-    """W warm-up steps, then K timed steps, each after an L2 flush, with the
-    four events rpa_forward_timed records around the planner, decode and
-    prefill kernels.  Returns per-step (step, plan, decode, prefill) ms and
-    the clocks sampled during the timed steps."""
+    """W warm-up steps, then two sets of K timed steps, each after an L2
+    flush.  The step time comes from the first set, bracketed by two events
+    on the launching stream only: the decode and prefill kernels are launched
+    as programmatic dependents of the kernel before them, and an event
+    between two kernels would serialise them.  The second set runs
+    rpa_forward_timed, whose four events around the planner, decode and
+    prefill kernels give each kernel's time (its sum is a little longer than
+    the first set's step).  Returns per-step ms lists and the clocks sampled
+    during both sets."""
     import ragged_paged_attention_kv_gb300 as rpa
     for _ in range(warmup):
         flush.zero_()
         step(ctx)
     if rpa.get_status(ctx["ws"]) != 0:
         raise RuntimeError(f"{ctx['w'].name}: device status nonzero after warm-up")
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    for e4 in evs:  # create the driver events before they are handed over
-        for e in e4:
-            e.record(stream)
+
+    def events(n, k):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(k)] for _ in range(n)]
+        for ev in evs:  # create the driver events before they are handed over
+            for e in ev:
+                e.record(stream)
+        return evs
+
+    outer, inner = events(steps, 2), events(steps, 4)
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     if rank == 0:
         clocks.start()
     barrier(world)
     for i in range(steps):
         flush.zero_()
-        step(ctx, events=evs[i])
+        outer[i][0].record(stream)
+        step(ctx)
+        outer[i][1].record(stream)
+    for i in range(steps):
+        flush.zero_()
+        step(ctx, events=inner[i])
     barrier(world)
     clk = clocks.stop() if rank == 0 else None
-    ms = {"step": [e[0].elapsed_time(e[3]) for e in evs],
-          "plan": [e[0].elapsed_time(e[1]) for e in evs],
-          "decode": [e[1].elapsed_time(e[2]) for e in evs],
-          "prefill": [e[2].elapsed_time(e[3]) for e in evs]}
+    ms = {"step": [e[0].elapsed_time(e[1]) for e in outer],
+          "plan": [e[0].elapsed_time(e[1]) for e in inner],
+          "decode": [e[1].elapsed_time(e[2]) for e in inner],
+          "prefill": [e[2].elapsed_time(e[3]) for e in inner],
+          "step_serialised": [e[0].elapsed_time(e[3]) for e in inner]}
     return ms, clk
 
 
@@ -421,7 +439,8 @@ def measure(name, args, world, rank, dev, flush, stream, with_e2e):
         "unit": "tokens/s", "tokens_per_step": tokens,
         "ms_per_step": round(total_s * 1e3 / args.steps, 4),
         "kernels_ms": {"plan": round(statistics.mean(ms["plan"]), 4),
-                       "decode": round(dec_avg, 4), "prefill": round(pf_avg, 4)},
+                       "decode": round(dec_avg, 4), "prefill": round(pf_avg, 4),
+                       "step_with_kernel_events": round(statistics.mean(ms["step_serialised"]), 4)},
         "bound": BOUNDS.get(name, "hbm" if not work["prefill"]["tokens"] else "tensor"),
         "rooflines": rooflines(w, work, dec_avg, pf_avg, peaks),
         "decode_kv_gbs": round(work["decode"]["bytes"] / (dec_avg * 1e-3) / 1e9, 1)

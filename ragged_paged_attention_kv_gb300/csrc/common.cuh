@@ -83,6 +83,22 @@ struct WorkspaceLayout {
   }
 };
 
+// ------------------------------------------------ programmatic launches
+// The decode and prefill kernels are launched as programmatic dependents of
+// the kernel before them on the stream, so their launch (and the planner's
+// successors' set-up) overlaps the kernel ahead.  griddep_wait blocks until
+// the preceding kernel has completed and its memory is visible; nothing a
+// dependent reads or writes in global memory may be touched before it.
+// Without a programmatic predecessor it returns at once.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel on the stream (if launched as a programmatic
+// dependent) begin launching before this grid completes.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- status
 __device__ __forceinline__ void set_status(int32_t* ws_header, int bits) {
   atomicOr(ws_header + kHdrStatus, bits);
@@ -124,10 +140,53 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// The same with fp16 A and B.
+__device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <bool F16>
+__device__ __forceinline__ void mma_p_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if (F16) mma_f16_16816(d, a, b0, b1); else mma_bf16_16816(d, a, b0, b1);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
   return *reinterpret_cast<uint32_t*>(&v);
+}
+// Two fp32 -> fp16 (round to nearest even, subnormals kept), packed low-first.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// The sum of the two values a packed pair holds (bf16 or fp16), in fp32:
+// the softmax normaliser is summed from exactly the weights the P V product
+// uses, so the output is a weighted mean of the values with weights that sum
+// to one (the rounding of P then moves the output by at most ~2^-8 times the
+// spread of the values around it, instead of 2^-9 times their magnitude).
+__device__ __forceinline__ float pair_sum_bf16(uint32_t u) {
+  return __uint_as_float(u << 16) + __uint_as_float(u & 0xFFFF0000u);
+}
+__device__ __forceinline__ float pair_sum_f16(uint32_t u) {
+  __half2 h = *reinterpret_cast<__half2*>(&u);
+  const float2 f = __half22float2(h);
+  return f.x + f.y;
+}
+// P (two softmax weights) packed for the P V product: bf16 when the values
+// are bf16, fp16 when they came from an e4m3 cache (every e4m3 value is
+// exact in fp16, and fp16 carries P with 3 more bits).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ float pair_sum(uint32_t u) {
+  return F16 ? pair_sum_f16(u) : pair_sum_bf16(u);
 }
 
 // Byte offset of 16-byte chunk `c` of row `r` in a tile whose rows are
@@ -187,6 +246,25 @@ __device__ __forceinline__ uint4 dequant8(uint2 codes) {
   r.z = e4m3x2_to_bf16x2((uint16_t)(codes.y & 0xFFFF));
   r.w = e4m3x2_to_bf16x2((uint16_t)(codes.y >> 16));
   return r;
+}
+// Two e4m3 codes -> two fp16 (exact: e4m3 has 3 mantissa bits and exponents
+// 2^-9 .. 2^8, all inside fp16), one conversion instruction.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+// 8 e4m3 codes -> 8 fp16 values (one 16-byte chunk).
+__device__ __forceinline__ uint4 dequant8_f16(uint2 codes) {
+  uint4 r;
+  r.x = e4m3x2_to_f16x2((uint16_t)(codes.x & 0xFFFF));
+  r.y = e4m3x2_to_f16x2((uint16_t)(codes.x >> 16));
+  r.z = e4m3x2_to_f16x2((uint16_t)(codes.y & 0xFFFF));
+  r.w = e4m3x2_to_f16x2((uint16_t)(codes.y >> 16));
+  return r;
+}
+template <bool F16>
+__device__ __forceinline__ uint4 dequant8_as(uint2 codes) {
+  return F16 ? dequant8_f16(codes) : dequant8(codes);
 }
 
 // ------------------------------------------------------------- reductions

@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.num_q_heads / p.num_kv_heads;
   const int P = p.page_size;
+  griddep_wait();  // the planner's unit list and counters are complete
+  griddep_launch_dependents();
   if (hdr[kHdrNumDecode] == 0) return;  // a prefill-only batch: nothing to set up
 
   // zero both query slots (rows >= G stay zero), init barriers; the bulk
@@ -342,17 +344,22 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
           const int r = rem / (Dp / 8), c = rem % (Dp / 8);
           const int j = kw + r;
           uint4 val;
+          // keys become bf16 (the queries' type), values fp16 (exact for
+          // e4m3, and the P V product then carries P in fp16)
           if (j < du.k_begin || j >= du.k_end || c >= D / 8) {
             val = make_uint4(0, 0, 0, 0);  // masked key, or a padding column
-          } else if (j == ctx) {
-            const __nv_bfloat16* in = (kv ? a.kv.values : a.kv.keys) +
-                                      ((int64_t)q0 * p.num_kv_heads + h) * D + c * 8;
-            val = dequant8(quantize8(__ldg(reinterpret_cast<const uint4*>(in)),
-                                     kv ? vs : ks));
           } else {
-            const uint2 codes = *reinterpret_cast<const uint2*>(
-                smem + (stage - s_base) + (2 * (warp * kKeysPerWarp + r) + kv) * C::kRowBytes + c * 8);
-            val = dequant8(codes);
+            uint2 codes;
+            if (j == ctx) {
+              const __nv_bfloat16* in = (kv ? a.kv.values : a.kv.keys) +
+                                        ((int64_t)q0 * p.num_kv_heads + h) * D + c * 8;
+              codes = quantize8(__ldg(reinterpret_cast<const uint4*>(in)), kv ? vs : ks);
+            } else {
+              codes = *reinterpret_cast<const uint2*>(
+                  smem + (stage - s_base) + (2 * (warp * kKeysPerWarp + r) + kv) * C::kRowBytes +
+                  c * 8);
+            }
+            val = kv ? dequant8_f16(codes) : dequant8(codes);
           }
           *reinterpret_cast<uint4*>((kv ? gV : gK) + swz(r, c, Dp * 2)) = val;
         }
@@ -432,17 +439,21 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
           rescale = true;
         }
       }
-      float rs[2] = {0.f, 0.f};
       const float ms0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
       const float ms1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pe = exp2f(sc[n][e] - ((e >> 1) ? ms1 : ms0));
-          sc[n][e] = pe;
-          rs[e >> 1] += pe;
-        }
+        for (int e = 0; e < 4; ++e) sc[n][e] = exp2f(sc[n][e] - ((e >> 1) ? ms1 : ms0));
+      // P as the P V product takes it (fp16 for an e4m3 cache, else bf16);
+      // the row sums add exactly those rounded weights
+      uint32_t pa[4];
+      pa[0] = pack_p<FP8>(sc[0][0], sc[0][1]);
+      pa[1] = pack_p<FP8>(sc[0][2], sc[0][3]);
+      pa[2] = pack_p<FP8>(sc[1][0], sc[1][1]);
+      pa[3] = pack_p<FP8>(sc[1][2], sc[1][3]);
+      const float rs[2] = {pair_sum<FP8>(pa[0]) + pair_sum<FP8>(pa[2]),
+                           pair_sum<FP8>(pa[1]) + pair_sum<FP8>(pa[3])};
       if (rescale) {
 #pragma unroll
         for (int n = 0; n < Dp / 8; ++n) {
@@ -454,11 +465,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + rs[r];
-      uint32_t pa[4];
-      pa[0] = pack_bf16(sc[0][0], sc[0][1]);
-      pa[1] = pack_bf16(sc[0][2], sc[0][3]);
-      pa[2] = pack_bf16(sc[1][0], sc[1][1]);
-      pa[3] = pack_bf16(sc[1][2], sc[1][3]);
 #pragma unroll
       for (int cp = 0; cp < Dp / 16; ++cp) {
         const int mi = lane >> 3;
@@ -467,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         const uint32_t addr = FP8 ? tV + swz(key, chunk, Dp * 2) : kv_addr(tV, key, 1, chunk);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * cp], pa, b0, b1);
-        mma_bf16_16816(o[2 * cp + 1], pa, b2, b3);
+        mma_p_16816<FP8>(o[2 * cp], pa, b0, b1);
+        mma_p_16816<FP8>(o[2 * cp + 1], pa, b2, b3);
       }
       // this warp's reads of the stage (and its edge stores) precede the
       // next TMA into it: the generic-to-async proxy fence orders them
@@ -618,8 +624,7 @@ static cudaError_t launch_decode_t(const AttnArgs& a, int max_units, int num_sms
   int grid = num_sms * C::kCtasPerSm;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
-  kern<<<grid, dec::kThreads, C::kBytes, stream>>>(maps, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, dec::kThreads, C::kBytes, stream, maps, a);
 }
 
 cudaError_t launch_decode(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream) {

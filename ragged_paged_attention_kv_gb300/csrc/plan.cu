@@ -128,6 +128,9 @@ __global__ void __launch_bounds__(kT) plan_kernel(rpa_params_t p, const int32_t*
   const int tid = threadIdx.x;
   const int Hkv = p.num_kv_heads, G = p.num_q_heads / p.num_kv_heads;
   const int tile_tokens = prefill_rows / G;  // new tokens per prefill tile
+  // the attention kernels launched behind this one may start their launch
+  // now; they wait for this grid to complete before reading its output
+  griddep_launch_dependents();
 
   // the first batch's metadata is loaded together with the distribution
   // (every index below max_num_seqs is inside the arrays)

@@ -58,9 +58,9 @@ __device__ __forceinline__ void load_tile(const AttnArgs& a, uint8_t* stage, int
       }
       const uint8_t* src =
           a.kv.cache + pool_offset(a.kv.p, page, j % a.kv.p.page_size, 2 * h + kv, FP8 ? 1 : 2);
-      if (FP8) {
+      if (FP8) {  // keys bf16, values fp16 (exact for e4m3)
         const uint2 codes = __ldg(reinterpret_cast<const uint2*>(src + c * 8));
-        *reinterpret_cast<uint4*>(dst) = dequant8(codes);
+        *reinterpret_cast<uint4*>(dst) = kv ? dequant8_f16(codes) : dequant8(codes);
       } else {
         cp_async_16(smem_u32(dst), src + c * 16);
       }
@@ -69,8 +69,8 @@ __device__ __forceinline__ void load_tile(const AttnArgs& a, uint8_t* stage, int
           (kv ? a.kv.values : a.kv.keys) + ((int64_t)(q0 + (j - ctx)) * Hkv + h) * D + c * 8;
       if (FP8) {
         const float scale = kv ? v_scale_of(a.kv.p, h) : k_scale_of(a.kv.p, h);
-        *reinterpret_cast<uint4*>(dst) =
-            dequant8(quantize8(__ldg(reinterpret_cast<const uint4*>(in)), scale));
+        const uint2 codes = quantize8(__ldg(reinterpret_cast<const uint4*>(in)), scale);
+        *reinterpret_cast<uint4*>(dst) = kv ? dequant8_f16(codes) : dequant8(codes);
       } else {
         cp_async_16(smem_u32(dst), in);
       }
@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
   const int gq = lane >> 2, tq = lane & 3;
   const int G = p.num_q_heads / p.num_kv_heads;
   const int W = p.sliding_window;
+  griddep_wait();  // the planner (and the decode kernel ahead) are complete
   const int n_units = hdr[kHdrNumPrefill];
 
   if (tid == 0) s_unit = atomicAdd(hdr + kHdrPrefillNext, 1);
@@ -229,14 +230,16 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
         alpha[r] = exp2f(m_run[r] - msafe[r]);
         m_run[r] = mnew;
       }
+      // P packed as the P V product takes it (fp16 with an e4m3 cache,
+      // else bf16); the row sums add exactly those rounded weights
       float rs[2] = {0.f, 0.f};
+      uint32_t pk[kBN / 8][2];
 #pragma unroll
       for (int n = 0; n < kBN / 8; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pe = exp2f(s[n][e] - msafe[e >> 1]);
-          s[n][e] = pe;
-          rs[e >> 1] += pe;
+        for (int r = 0; r < 2; ++r) {
+          pk[n][r] = pack_p<FP8>(exp2f(s[n][2 * r] - msafe[r]), exp2f(s[n][2 * r + 1] - msafe[r]));
+          rs[r] += pair_sum<FP8>(pk[n][r]);
         }
 #pragma unroll
       for (int r = 0; r < 2; ++r) l_run[r] = l_run[r] * alpha[r] + rs[r];
@@ -249,11 +252,8 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
       }
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-        pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-        pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+        const uint32_t pa[4] = {pk[2 * kk][0], pk[2 * kk][1], pk[2 * kk + 1][0],
+                                pk[2 * kk + 1][1]};
 #pragma unroll
         for (int cp = 0; cp < Dp / 16; ++cp) {
           const int mi = lane >> 3;
@@ -261,8 +261,8 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
           const int chunk = 2 * cp + (mi >> 1);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4_trans(smem_u32(tV + swz(key, chunk, Dp * 2)), b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * cp], pa, b0, b1);
-          mma_bf16_16816(o[2 * cp + 1], pa, b2, b3);
+          mma_p_16816<FP8>(o[2 * cp], pa, b0, b1);
+          mma_p_16816<FP8>(o[2 * cp + 1], pa, b2, b3);
         }
       }
       __syncthreads();  // the stage is refilled next iteration
@@ -321,8 +321,7 @@ static cudaError_t launch_prefill_t(const AttnArgs& a, int max_units, int num_sm
   int grid = num_sms * per_sm;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
-  kern<<<grid, pf::kThreads, S::kBytes, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, pf::kThreads, S::kBytes, stream, a);
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream) {

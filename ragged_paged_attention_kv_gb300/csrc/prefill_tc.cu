@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.num_q_heads / p.num_kv_heads;
   const int P = p.page_size;
   const int W = p.sliding_window;
+  griddep_wait();  // the planner (and the decode kernel ahead) are complete
   const int n_units = hdr[kHdrNumPrefill];
   if (n_units == 0) return;  // a decode-only batch: nothing to set up
 
@@ -207,7 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem;
 
   const uint32_t idesc_qk = idesc_bf16(kM, kN, false, false);
-  const uint32_t idesc_pv = idesc_bf16(kM, D, false, true);
+  // P and the values are fp16 with an e4m3 cache, bf16 otherwise
+  const uint32_t idesc_pv = idesc_bf16(kM, D, false, true, FP8);
   const bool has_cap = p.logits_soft_cap > 0.f;
   // the logit transform of the scalar key scale (used unless per-head scales)
   const LogitXform xf0 = make_xform(p.softmax_scale, p.k_scale, p.logits_soft_cap);
@@ -239,12 +241,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = 32 * part + lane; idx < rows * (D / 8); idx += 32 * kDecWarps) {
       const int r = idx / (D / 8), c = idx % (D / 8);
       uint4* dst = reinterpret_cast<uint4*>(op + (c >> 3) * kHalf + sw128(r, c & 7));
+      // keys become bf16 (the queries' type); values fp16, exact for e4m3,
+      // so that the P V product carries P in fp16
       if (r >= valid || r < lead) {
         *dst = make_uint4(0, 0, 0, 0);
       } else if (is_new) {
-        *dst = dequant8(quantize8(*dst, scale));
+        const uint2 codes = quantize8(*dst, scale);
+        *dst = kv ? dequant8_f16(codes) : dequant8(codes);
       } else {
-        *dst = dequant8(*reinterpret_cast<const uint2*>(stg + r * D + c * 8));
+        const uint2 codes = *reinterpret_cast<const uint2*>(stg + r * D + c * 8);
+        *dst = kv ? dequant8_f16(codes) : dequant8(codes);
       }
     }
   };
@@ -613,7 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float nm = m_run == -INFINITY ? 0.f : -m_run;
         const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(nm, nm);
         uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-        // P packed as bf16 pairs into sr[0..64): sr[c/2] is already consumed.
+        // P packed as pairs into sr[0..64): sr[c/2] is already consumed.
+        // bf16 pairs, or fp16 with an e4m3 cache (the values' type).  The row
+        // sums add the rounded weights, exactly those the P V product uses.
         // Scale-and-subtract and the row sums use packed f32x2 arithmetic
         // (one instruction per pair), the exponentials the hardware ex2.
 #pragma unroll
@@ -622,9 +630,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nm2);
           float x0, x1;
           f2_unpack(x2, x0, x1);
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          rs2[(c >> 1) & 1] = f2_add(rs2[(c >> 1) & 1], f2_pack(p0, p1));
-          sr[c >> 1] = pack_bf16(p0, p1);
+          const uint32_t pk = pack_p<FP8>(fast_exp2(x0), fast_exp2(x1));
+          float r0, r1;
+          if (FP8) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk));
+            r0 = f.x;
+            r1 = f.y;
+          } else {
+            r0 = __uint_as_float(pk << 16);
+            r1 = __uint_as_float(pk & 0xFFFF0000u);
+          }
+          rs2[(c >> 1) & 1] = f2_add(rs2[(c >> 1) & 1], f2_pack(r0, r1));
+          sr[c >> 1] = pk;
         }
         {
           float a0, a1, b0, b1;
@@ -703,8 +720,7 @@ static cudaError_t launch_prefill_tc_t(const AttnArgs& a, int max_units, int num
   int grid = num_sms;
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
-  kern<<<grid, tc::kThreads, C::kSmemBytes, stream>>>(maps, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, tc::kThreads, C::kSmemBytes, stream, maps, a);
 }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream) {

@@ -43,11 +43,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulate.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor for kind::f16 with bf16 A/B (or, with f16 = true,
+// fp16 A/B: both operands always share one type) and fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                  bool f16 = false) {
   return (1u << 4)                      // D format: f32
-         | (1u << 7)                    // A format: bf16
-         | (1u << 10)                   // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)       // A format: bf16 (1) or f16 (0)
+         | ((f16 ? 0u : 1u) << 10)      // B format: bf16 (1) or f16 (0)
          | ((a_mn_major ? 1u : 0u) << 15)
          | ((b_mn_major ? 1u : 0u) << 16)
          | ((uint32_t)(N >> 3) << 17)

@@ -67,11 +67,17 @@ def output_errors(got: np.ndarray, exact: np.ndarray):
 def assert_close(got, exact, what=""):
     """Asserts the stated bounds; returns (max raw error, mean raw error)."""
     got = np.asarray(got, np.float64)
+    exact = np.asarray(exact, np.float64)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     ratio, mean, raw = output_errors(got, exact)
+    where = ""
+    if ratio > 1.0:
+        r = np.abs(got - exact) / max_abs_bound(exact)
+        i = np.unravel_index(int(np.argmax(r)), r.shape)
+        where = f"; worst at index {tuple(int(x) for x in i)}: got {got[i]:.6g}, exact {exact[i]:.6g}"
     assert ratio <= 1.0 and mean <= MEAN_ABS_TOL, \
         f"{what}: max abs err {raw:.4g} (bound 1e-2 below |exact| 4, ulp/2 + 1e-2 above; " \
-        f"worst ratio {ratio:.3g}), mean abs err {mean:.3g} (tol {MEAN_ABS_TOL})"
+        f"worst ratio {ratio:.3g}), mean abs err {mean:.3g} (tol {MEAN_ABS_TOL}){where}"
     return raw, mean
 
 
