@@ -253,10 +253,13 @@ def job_throughput(tokens_per_step: int, world: int, steps: int, seconds: float)
 
 
 def prefill_kernel_name(w):
-    """The prefill kernel the library runs for this workload's shape."""
-    g = w.num_q_heads // w.num_kv_heads
-    if w.head_dim in (64, 128) and w.page_size >= 8 and g <= 16:
+    """The prefill kernel the library runs for this workload's shape: the
+    tcgen05 kernels for pages of at least 8 rows (two query tiles per unit at
+    head_dim 64/128, one at 192/256), else the warp-level MMA kernel."""
+    if w.page_size >= 8 and w.head_dim in (64, 128):
         return "prefill_tc_kernel", "prefill_tc.cu"
+    if w.page_size >= 8 and w.head_dim in (192, 256):
+        return "prefill_tc_wide_kernel", "prefill_tc_wide.cu"
     return "prefill_kernel", "prefill.cu"
 
 

@@ -72,7 +72,7 @@ namespace rpa {
 int enqueue_forward(const rpa_params_t& p, const AttnArgs& a, const int32_t* distribution,
                     int num_sms, cudaStream_t s, void* const* events) {
   const WorkspaceLayout L(p);
-  const bool tc = prefill_uses_tc(p);
+  const PrefillKind kind = prefill_kind(p);
   auto mark = [&](int i) -> bool {
     return !events || cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
   };
@@ -83,8 +83,10 @@ int enqueue_forward(const rpa_params_t& p, const AttnArgs& a, const int32_t* dis
   if (!mark(1)) return RPA_ERR_CUDA;
   if (launch_decode(a, (int)L.max_decode_units, num_sms, s) != cudaSuccess) return RPA_ERR_CUDA;
   if (!mark(2)) return RPA_ERR_CUDA;
-  const cudaError_t e = tc ? launch_prefill_tc(a, (int)L.max_prefill_units, num_sms, s)
-                           : launch_prefill(a, (int)L.max_prefill_units, num_sms, s);
+  const int mu = (int)L.max_prefill_units;
+  const cudaError_t e = kind == kPrefillTc       ? launch_prefill_tc(a, mu, num_sms, s)
+                        : kind == kPrefillTcWide ? launch_prefill_tc_wide(a, mu, num_sms, s)
+                                                 : launch_prefill(a, mu, num_sms, s);
   if (e != cudaSuccess) return RPA_ERR_CUDA;
   if (!mark(3)) return RPA_ERR_CUDA;
   return RPA_OK;

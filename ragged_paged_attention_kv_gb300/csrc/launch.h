@@ -13,11 +13,23 @@ cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int
 cudaError_t launch_cache_write(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,
                                int prefill_rows, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
-// warp-level MMA prefill (64-row tiles): pages of fewer than 8 rows, and head_dim 96/192/256
+// The prefill kernel for these params:
+//   kPrefillTc      tcgen05, two 128-row query tiles per unit: head_dim 64 and 128
+//   kPrefillTcWide  tcgen05, one 128-row query tile per unit: head_dim 192 and 256
+//   kPrefillMma     warp-level MMA, 64-row tiles: head_dim 96, and pages of
+//                   fewer than 8 rows (the tcgen05 kernels' TMA warp holds
+//                   one page of a key tile per lane)
+enum PrefillKind { kPrefillMma = 0, kPrefillTc = 1, kPrefillTcWide = 2 };
+inline PrefillKind prefill_kind(const rpa_params_t& p) {
+  if (p.page_size < 8) return kPrefillMma;
+  if (p.head_dim == 64 || p.head_dim == 128) return kPrefillTc;
+  if (p.head_dim == 192 || p.head_dim == 256) return kPrefillTcWide;
+  return kPrefillMma;
+}
 cudaError_t launch_prefill(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
-// tcgen05 prefill (two 128-row query tiles per unit): head_dim 64 and 128, pages >= 8 rows
-bool prefill_uses_tc(const rpa_params_t& p);
 cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);
+cudaError_t launch_prefill_tc_wide(const AttnArgs& a, int max_units, int num_sms,
+                                   cudaStream_t stream);
 
 // The alignment the kernels' bulk and tensor copies rely on: the bf16
 // tensors and the cache on 16 bytes, the int32 arrays and the sink on 4.
@@ -32,8 +44,14 @@ inline bool pointers_aligned(const void* queries, const void* keys, const void* 
          on(attention_sink, 4);
 }
 
-// Rows of a prefill tile for these params (the planner and the kernels agree on it).
-inline int prefill_rows_for(const rpa_params_t& p) { return prefill_uses_tc(p) ? 256 : kPrefillRows; }
+// Rows of a prefill unit for these params (the planner and the kernels agree on it).
+inline int prefill_rows_for(const rpa_params_t& p) {
+  switch (prefill_kind(p)) {
+    case kPrefillTc: return 256;
+    case kPrefillTcWide: return 128;
+    default: return kPrefillRows;
+  }
+}
 
 // plan -> decode -> prefill on `stream`; events (4, or null) are recorded
 // before the planner and after each kernel.

@@ -33,6 +33,7 @@
 #include "async.cuh"
 #include "common.cuh"
 #include "kv_write.cuh"
+#include "launch.h"
 #include "tcgen05.cuh"
 #include "tma_host.h"
 
@@ -688,11 +689,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace tc
-
-bool prefill_uses_tc(const rpa_params_t& p) {
-  const int G = p.num_q_heads / p.num_kv_heads;
-  return (p.head_dim == 64 || p.head_dim == 128) && p.page_size >= 8 && G >= 1 && G <= 16;
-}
 
 template <int D, bool FP8, bool PH>
 static cudaError_t launch_prefill_tc_t(const AttnArgs& a, int max_units, int num_sms,

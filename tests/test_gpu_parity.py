@@ -250,15 +250,65 @@ POISON_CASES = [
                                                  head_dim=128, sliding_window=77)),
     ("mma_prefill_p4_window", lambda: _case("z10", 310, [1, 25, 9], [90, 60, 40], page_size=4,
                                             sliding_window=20)),
-    ("mma_prefill_d256_fp8_window", lambda: _case("z11", 311, [1, 70, 8], [900, 200, 8],
+    ("mma_prefill_d256_p4_window", lambda: _case("z11", 311, [1, 70, 8], [900, 200, 8],
+                                                 head_dim=256, page_size=4, sliding_window=50)),
+    ("tcw_prefill_d256_fp8_window", lambda: _case("z12", 312, [1, 70, 8], [900, 200, 8],
                                                   kv_dtype="fp8", head_dim=256, k_scale=0.05,
                                                   v_scale=0.07, sliding_window=50)),
+    ("tcw_prefill_d192_partial_pages", lambda: _case("z13", 313, [130, 1, 7], [1000, 70, 135],
+                                                     head_dim=192, num_q_heads=16,
+                                                     num_kv_heads=8, page_size=64,
+                                                     sliding_window=300)),
 ]
 
 
 @pytest.mark.parametrize("name,make", POISON_CASES, ids=[c[0] for c in POISON_CASES])
 def test_nonfinite_bytes_in_unread_slots(name, make):
     check_case(make(), poison=True)
+
+
+def _tcw(name, seed, q_lens, kv_lens, **kw):
+    """A case for the tcgen05 prefill at head_dim 192/256 (one query tile per
+    unit, 64-key tiles, S double-buffered in tensor memory)."""
+    base = dict(num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=16)
+    base.update(kw)
+    return wl.make_custom(name, seed, q_lens, kv_lens, **base)
+
+
+TCW_CASES = [
+    ("p8", lambda: _tcw("w8", 401, [1, 90, 13], [70, 400, 141], page_size=8)),
+    ("p128", lambda: _tcw("w128", 402, [1, 200, 7], [900, 700, 135], page_size=128)),
+    ("d192_p256_partial_pages", lambda: _tcw("w256p", 403, [150, 40], [1000, 40], head_dim=192,
+                                             page_size=256)),
+    ("gqa1_long_tiles", lambda: _tcw("wg1", 404, [300, 129, 1], [900, 129, 50], num_q_heads=4,
+                                     num_kv_heads=4)),
+    ("gqa16", lambda: _tcw("wg16", 405, [1, 37, 9], [260, 300, 9], num_q_heads=32,
+                           num_kv_heads=2)),
+    ("window_in_cached_tiles", lambda: _tcw("ww", 406, [1, 100, 64], [2000, 1500, 64],
+                                            sliding_window=200)),
+    ("window_short", lambda: _tcw("wws", 407, [70, 1], [600, 333], sliding_window=5)),
+    ("softcap_sink", lambda: _tcw("wcs", 408, [1, 90, 33], [500, 300, 33], logits_soft_cap=7.5,
+                                  has_sink=True, softmax_scale=0.2)),
+    ("ctx_tile_aligned", lambda: _tcw("wca", 409, [128, 1], [384, 129], page_size=32)),
+    ("many_tiles_ragged", lambda: _tcw("wmr", 410, [517, 3, 1], [1800, 700, 60], page_size=64,
+                                       head_dim=192)),
+    ("fp8_options", lambda: _tcw("wf8", 411, [1, 1, 64, 20], [900, 129, 200, 20], kv_dtype="fp8",
+                                 k_scale=0.05, v_scale=0.07, logits_soft_cap=30.0, has_sink=True,
+                                 sliding_window=128)),
+    ("fp8_d192_per_head", lambda: _tcw("wf8h", 412, [1, 90, 33], [600, 500, 33], head_dim=192,
+                                       kv_dtype="fp8", k_scale_heads=[0.02, 0.05, 0.11, 0.3,
+                                                                      0.04, 0.07, 0.2, 0.09],
+                                       v_scale_heads=[0.07, 0.015, 0.2, 0.05, 0.1, 0.03, 0.06,
+                                                      0.12])),
+    ("fp8_new_tokens_only", lambda: _tcw("wf8n", 413, [200, 70], [200, 70], kv_dtype="fp8",
+                                         k_scale=0.3, v_scale=0.1, num_q_heads=8,
+                                         num_kv_heads=2)),
+]
+
+
+@pytest.mark.parametrize("name,make", TCW_CASES, ids=[c[0] for c in TCW_CASES])
+def test_tcgen05_wide_prefill_cases(name, make):
+    check_case(make())
 
 
 def test_decode_split_boundaries():
@@ -581,6 +631,6 @@ def test_full_fp8_workload():
                       batch=64) == 512
 
 
-@pytest.mark.parametrize("name", ["long", "long_w4096"])
+@pytest.mark.parametrize("name", ["long", "long_w4096", "long_d256"])
 def test_full_long_workload(name):
     _full_size(name, prefill_seqs=[0, 1], sample_tokens_per_seq=6)
