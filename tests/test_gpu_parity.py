@@ -200,6 +200,10 @@ TC_CASES = [
     ("window_in_cached_tiles", lambda: _tc("tw", 207, [1, 100, 64], [2000, 1500, 64],
                                            sliding_window=200)),
     ("window_short", lambda: _tc("tws", 208, [70, 1], [600, 333], sliding_window=5)),
+    # windows above 256 keys stay on the tcgen05 kernel (shorter ones run on
+    # the warp-level kernel): a window start inside a cached tile
+    ("window_300_cached", lambda: _tc("tw3", 212, [1, 100, 64, 300], [2000, 1500, 64, 900],
+                                      sliding_window=300)),
     ("softcap_sink", lambda: _tc("tcs", 209, [1, 90, 33], [500, 300, 33], logits_soft_cap=7.5,
                                  has_sink=True, softmax_scale=0.2)),
     ("ctx_tile_aligned", lambda: _tc("tca", 210, [128, 1], [384, 129], page_size=32)),
@@ -250,6 +254,17 @@ POISON_CASES = [
                                                  head_dim=128, sliding_window=77)),
     ("mma_prefill_p4_window", lambda: _case("z10", 310, [1, 25, 9], [90, 60, 40], page_size=4,
                                             sliding_window=20)),
+    # windows above 256 keys: the tcgen05 kernels (bf16 and fp8 staging)
+    ("tc_prefill_window_300", lambda: _tc("z14", 314, [1, 100, 64, 300], [2000, 1500, 64, 900],
+                                          sliding_window=300)),
+    ("tc_prefill_fp8_window_300", lambda: _case("z15", 315, [1, 1, 64, 20], [900, 129, 800, 20],
+                                                kv_dtype="fp8", k_scale=0.05, v_scale=0.07,
+                                                num_q_heads=64, num_kv_heads=8,
+                                                logits_soft_cap=30.0, has_sink=True,
+                                                sliding_window=300)),
+    ("tcw_prefill_d256_fp8_window_260", lambda: _case("z16", 316, [1, 70, 8], [900, 600, 8],
+                                                      kv_dtype="fp8", head_dim=256, k_scale=0.05,
+                                                      v_scale=0.07, sliding_window=260)),
     ("mma_prefill_d256_p4_window", lambda: _case("z11", 311, [1, 70, 8], [900, 200, 8],
                                                  head_dim=256, page_size=4, sliding_window=50)),
     ("tcw_prefill_d256_fp8_window", lambda: _case("z12", 312, [1, 70, 8], [900, 200, 8],
@@ -287,6 +302,11 @@ TCW_CASES = [
     ("window_in_cached_tiles", lambda: _tcw("ww", 406, [1, 100, 64], [2000, 1500, 64],
                                             sliding_window=200)),
     ("window_short", lambda: _tcw("wws", 407, [70, 1], [600, 333], sliding_window=5)),
+    ("window_300_cached", lambda: _tcw("ww3", 414, [1, 100, 64, 200], [2000, 1500, 64, 900],
+                                       sliding_window=300)),
+    ("fp8_window_270", lambda: _tcw("wf82", 415, [1, 90, 20], [900, 700, 20], kv_dtype="fp8",
+                                    k_scale=0.05, v_scale=0.07, logits_soft_cap=30.0,
+                                    has_sink=True, sliding_window=270)),
     ("softcap_sink", lambda: _tcw("wcs", 408, [1, 90, 33], [500, 300, 33], logits_soft_cap=7.5,
                                   has_sink=True, softmax_scale=0.2)),
     ("ctx_tile_aligned", lambda: _tcw("wca", 409, [128, 1], [384, 129], page_size=32)),
