@@ -32,9 +32,10 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _flags(extra=()):
+def _flags(extra=(), defines=None):
     # RPA_NVCC_DEFINES: extra -D options (e.g. "-DRPA_DECODE_UNITS_TARGET=2048") for tuning builds
-    defines = os.environ.get("RPA_NVCC_DEFINES", "").split()
+    if defines is None:
+        defines = os.environ.get("RPA_NVCC_DEFINES", "").split()
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                    "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr", *defines, *extra]
 
@@ -50,9 +51,9 @@ def _stale(obj, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src, obj, verbose, ptxas_verbose):
+def _compile(src, obj, verbose, ptxas_verbose, defines=None):
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
-    cmd = [_nvcc(), *_flags(extra), "-c", src, "-o", obj]
+    cmd = [_nvcc(), *_flags(extra, defines), "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stderr}")
@@ -61,33 +62,43 @@ def _compile(src, obj, verbose, ptxas_verbose):
     return r.stderr
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          variant: str = None, defines=None) -> str:
+    """Builds librpa.so; with `variant` (a name) and `defines` (-D options), a
+    separate copy built with those options under _build/variants/<name>/ --
+    for tests that need a build-time setting the product never uses (a
+    short wait limit, say).  Returns the library's path."""
+    obj_dir, lib = OBJ_DIR, LIB
+    if variant is not None:
+        obj_dir = os.path.join(OBJ_DIR, "variants", variant)
+        lib = os.path.join(obj_dir, "librpa.so")
+        defines = list(defines or [])
+    os.makedirs(obj_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = _headers()
     jobs = []
     objs = []
     for src in sources:
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or ptxas_verbose or _stale(obj, [src, *headers]):
             jobs.append((src, obj))
     logs = []
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
-            futs = [ex.submit(_compile, s, o, verbose, ptxas_verbose) for s, o in jobs]
+            futs = [ex.submit(_compile, s, o, verbose, ptxas_verbose, defines) for s, o in jobs]
             for f in futs:
                 logs.append(f.result())
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".{os.getpid()}.tmp"
         cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
     if ptxas_verbose:
         print("\n".join(logs))
-    return LIB
+    return lib
 
 
 def main(argv=None):

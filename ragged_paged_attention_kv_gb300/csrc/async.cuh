@@ -12,7 +12,17 @@
 
 namespace rpa {
 
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+// Limit of every bounded wait.  A test build sets a short one (and can make
+// one wait never complete) to exercise the timeout path.
+#ifndef RPA_WAIT_LIMIT_NS
+#define RPA_WAIT_LIMIT_NS 2000000000ull  // 2 s
+#endif
+constexpr unsigned long long kWaitLimitNs = RPA_WAIT_LIMIT_NS;
+// Test builds only: when nonzero, the producers never signal that the query
+// tile of a unit has landed, so the first wait on it runs out.
+#ifndef RPA_TEST_STALL_QUERY
+#define RPA_TEST_STALL_QUERY 0
+#endif
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
@@ -68,6 +78,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (*abort) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// Waits for the phase of parity `parity` without looking at the abort flag:
+// an aborting CTA uses it to let the asynchronous copies and tensor-core
+// products it issued finish before it frees their shared or tensor memory
+// and exits.  Bounded by the same limit; false if it gave up.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// All threads of named barrier `id` (count threads) vote: true iff every
+// one of them passes true.  Used where threads must leave a loop together
+// (a thread that left alone would leave the others waiting at the next
+// named barrier, which has no time limit).
+__device__ __forceinline__ bool named_bar_all(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // ------------------------------------------------------------------ TMA

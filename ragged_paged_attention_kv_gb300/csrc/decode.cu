@@ -162,6 +162,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
     const int n_units = hdr[kHdrNumDecode];
     const int rows = P < kBN ? P : kBN;  // rows of one box
     uint32_t g = 0;                      // stages issued so far
+    uint32_t nq = 0;                     // query-slot copies issued so far
+    bool ended = false;                  // the "no more units" signal was posted
     bool ok = true;
     for (uint32_t uq = 0; ok; ++uq) {
       const int slot = uq & 1;
@@ -204,8 +206,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
           info[slot].du.seq = -1;
           mbar_arrive(bar_qfull + 8 * slot);
         }
+        ended = true;
         break;
       }
+      constexpr bool kIssueQ = RPA_TEST_STALL_QUERY == 0;
       if (lane == 0) {
         UnitInfo ui;
         ui.du = du;
@@ -214,19 +218,20 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         ui.ctx = kv_len - 1;
         info[slot] = ui;
         const uint32_t qbytes = (uint32_t)(G * D * 2);
-        mbar_arrive_expect_tx(bar_qfull + 8 * slot, qbytes);
-        if (!C::kQPerRow)
+        if (kIssueQ) mbar_arrive_expect_tx(bar_qfull + 8 * slot, qbytes);
+        if (kIssueQ && !C::kQPerRow)
           bulk_load(s_base + C::kOffQ + slot * C::kQBytes,
                     a.queries + ((int64_t)q0 * p.num_q_heads + du.head * G) * D, qbytes,
                     bar_qfull + 8 * slot);
       }
-      if (C::kQPerRow) {  // one row per lane at the padded stride
-        __syncwarp();       // the expected bytes are posted first
+      if (kIssueQ && C::kQPerRow) {  // one row per lane at the padded stride
+        __syncwarp();                // the expected bytes are posted first
         if (lane < G)
           bulk_load(s_base + C::kOffQ + slot * C::kQBytes + lane * C::kQRow,
                     a.queries + ((int64_t)q0 * p.num_q_heads + du.head * G + lane) * D,
                     (uint32_t)(D * 2), bar_qfull + 8 * slot);
       }
+      if (kIssueQ) ++nq;
       for (int st = 0; st < n_st; ++st, ++g) {
         int ids[2] = {ids_next[0], ids_next[1]};
         if (st + 1 < n_st) load_ids(st + 1, ids_next);
@@ -264,6 +269,21 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       set_status(hdr, RPA_STATUS_TIMEOUT);
       s_abort = 1;
     }
+    // Let every copy this warp issued land before the CTA may exit (on an
+    // abort the consumers stop waiting for them): the last query copy of
+    // each slot and the last stage of each ring slot.  A slot's earlier
+    // copies completed before it was refilled -- by a later unit, or by the
+    // "no more units" signal, which also completes a phase of the slot's
+    // barrier (so the copy before it must not be waited on by parity).
+    if (lane == 0) {
+      bool drained = true;
+      for (uint32_t i = nq > 2 ? nq - 2 : 0; i < nq; ++i)
+        if (!(ended && i + 2 == nq))
+          drained &= mbar_drain(bar_qfull + 8 * (i & 1), (i >> 1) & 1);
+      for (uint32_t i = g > (uint32_t)C::kStages ? g - C::kStages : 0; i < g; ++i)
+        drained &= mbar_drain(bar_full + 8 * (i % C::kStages), (i / C::kStages) & 1);
+      if (!drained) set_status(hdr, RPA_STATUS_TIMEOUT);
+    }
     return;
   }
 
@@ -272,8 +292,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
   uint32_t g = 0;
   for (uint32_t uq = 0;; ++uq) {
     const int slot = uq & 1;
-    if (!mbar_wait(bar_qfull + 8 * slot, (uq >> 1) & 1, &s_abort)) {
-      set_status(hdr, RPA_STATUS_TIMEOUT);
+    // the consumer warps leave together or not at all: a warp that left
+    // alone would leave the others at the next named barrier
+    const bool q_ok = mbar_wait(bar_qfull + 8 * slot, (uq >> 1) & 1, &s_abort);
+    if (!named_bar_all(1, kConsumerWarps * 32, q_ok)) {
+      if (!q_ok && lane == 0) set_status(hdr, RPA_STATUS_TIMEOUT);
       s_abort = 1;
       break;
     }
@@ -487,12 +510,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_qempty + 8 * slot);
     }
-    if (!ok) {
-      set_status(hdr, RPA_STATUS_TIMEOUT);
-      s_abort = 1;
-      break;
-    }
-
     if (du.split == 0 && warp == 0) token_kv_store<FP8, D>(a.kv, tkv, ctx, h, lane);
 
     // per-warp state -> shared memory rows [warp][row] of (m, l, O[D]); only
@@ -516,7 +533,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
           *reinterpret_cast<float2*>(row + 2 + n * 8 + 2 * tq) = make_float2(o[n][2], o[n][3]);
       }
     }
-    named_bar(1, kConsumerWarps * 32);
+    // the barrier before the merge is also a vote: the consumer warps go on
+    // only if every one of them saw all its stages, else all leave together
+    if (!named_bar_all(1, kConsumerWarps * 32, ok)) {
+      if (!ok && lane == 0) set_status(hdr, RPA_STATUS_TIMEOUT);
+      s_abort = 1;
+      break;
+    }
 
     const bool single = du.nsplit == 1;
     const int ctid = tid;  // consumers are threads 0..127

@@ -91,7 +91,8 @@ enum Bar {
   kBarSFull = 13,   // [2] per query tile: S computed
   kBarPReady = 15,  // [2] per query tile: P written (and O corrected)
   kBarODone = 17,   // [2] per query tile: the unit's last PV product done
-  kNumBars = 19,
+  kBarDrain = 19,   // once, at exit: every tcgen05 product the MMA thread issued is done
+  kNumBars = 20,
 };
 
 struct TcMaps {
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarPReady + s), 4);
       mbar_init(bar(kBarODone + s), 1);
     }
+    mbar_init(bar(kBarDrain), 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -276,6 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
     if (warp == 0) {
+      // the last query copy (unit count) and the last key / value copy (tile
+      // count) per stage this warp issued, for the drain at exit
+      int q_last = -1, k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
       unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t ucount) {
       const int nt = g.n_tiles;
       // ------------------------------------------------------- TMA producer
@@ -283,12 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // j-2 are done; values into value stage j%2 once both PV products of
       // tile j-2 are done; after the values of a tile land, rows outside its
       // valid range are zeroed.
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kBarQFull), 2 * kOperand);
-        for (int x = 0; x < 2; ++x)
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_3d(sb + kOffQ + x * kOperand + hf * kHalf, &maps.q, bar(kBarQFull),
-                        hf * 64, g.h * G, g.q0 + g.t_begin + x * (kM / G));
+      if (RPA_TEST_STALL_QUERY == 0) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(kBarQFull), 2 * kOperand);
+          for (int x = 0; x < 2; ++x)
+            for (int hf = 0; hf < C::kHalves; ++hf)
+              tma_load_3d(sb + kOffQ + x * kOperand + hf * kHalf, &maps.q, bar(kBarQFull),
+                          hf * 64, g.h * G, g.q0 + g.t_begin + x * (kM / G));
+        }
+        q_last = (int)ucount;
       }
       // Page ids of a cached tile: lane l holds page pg0 + l (a tile spans at
       // most 128/P + 1 <= 17 pages for P >= 8), loaded one tile ahead so the
@@ -408,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         issue(j, 0, tc, ids);
+        k_last[s] = (int)tc;
         if (FP8 && !kStg1 && j >= 1) {
           ok = finalize_k(tc - 1, j - 1);
           if (!ok) break;
@@ -422,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         issue(j, 1, tc, ids);
+        v_last[s] = (int)tc;
         __syncwarp();
         if (!kStg1 && j >= 1) ok = finalize_v(tc - 1, j - 1);
       }
@@ -432,6 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_abort = 1;
       }
       });
+      // every copy this warp issued lands before the CTA may free its shared
+      // memory: an aborted unit leaves copies nobody waits for
+      if (lane == 0) {
+        bool drained = q_last < 0 || mbar_drain(bar(kBarQFull), q_last & 1);
+        for (int s = 0; s < 2; ++s) {
+          if (k_last[s] >= 0) drained &= mbar_drain(bar(kBarKFull + s), (k_last[s] >> 1) & 1);
+          if (v_last[s] >= 0) drained &= mbar_drain(bar(kBarVFull + s), (v_last[s] >> 1) & 1);
+        }
+        if (!drained) set_status(hdr, RPA_STATUS_TIMEOUT);
+      }
     } else if (warp == 1) {
       unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t ucount) {
       const int nt = g.n_tiles;
@@ -496,6 +516,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       });
+      // every product this thread issued completes before tensor memory is
+      // freed (an aborted unit can leave some in flight)
+      if (lane == 0) {
+        umma_commit(bar(kBarDrain));
+        if (!mbar_drain(bar(kBarDrain), 0)) set_status(hdr, RPA_STATUS_TIMEOUT);
+      }
     } else {
       if (FP8) {
         // warps 2 and 3: their shares of the fp8 decoding, tile by tile

@@ -80,7 +80,8 @@ enum Bar {
   kBarPReady = 15,  // [2] per S slot: P written (and O corrected)
   kBarPVDone = 17,  // every P V product done, in order (for O rescales)
   kBarODone = 18,   // the unit's last P V product done
-  kNumBars = 19,
+  kBarDrain = 19,   // once, at exit: every tcgen05 product the MMA thread issued is done
+  kNumBars = 20,
 };
 
 struct Maps {
@@ -180,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kBarPVDone), 1);
     mbar_init(bar(kBarODone), 1);
+    mbar_init(bar(kBarDrain), 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -253,14 +255,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
+    // the last query copy (unit count) and the last key / value copy (tile
+    // count) per stage this warp issued, for the drain at exit
+    int q_last = -1, k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
     unit_loop([&](const Geom& g, const uint32_t tcount, const uint32_t ucount) {
       const int nt = g.n_tiles;
       // ----------------------------------------------------- TMA producer
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kBarQFull), C::kQBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(sb + C::kOffQ + hf * kHalfQ, &maps.q, bar(kBarQFull), hf * 64, g.h * G,
-                      g.q0 + g.t_begin);
+      if (RPA_TEST_STALL_QUERY == 0) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(kBarQFull), C::kQBytes);
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(sb + C::kOffQ + hf * kHalfQ, &maps.q, bar(kBarQFull), hf * 64, g.h * G,
+                        g.q0 + g.t_begin);
+        }
+        q_last = (int)ucount;
       }
       // page ids of a cached tile: lane l holds page pg0 + l (a 64-key tile
       // spans at most 64/P <= 8 pages for P >= 8), loaded one tile ahead
@@ -373,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         issue(j, 0, tc, ids);
+        k_last[s] = (int)tc;
         if (FP8 && j >= 1) {
           ok = finalize_v(tc - 1, j - 1) &&
                mbar_wait(bar(kBarVReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
@@ -383,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         issue(j, 1, tc, ids);
+        v_last[s] = (int)tc;
         __syncwarp();
         if (!FP8 && j >= 1) ok = finalize_v(tc - 1, j - 1);
       }
@@ -393,6 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_abort = 1;
       }
     });
+    // every copy this warp issued lands before the CTA may free its shared
+    // memory: an aborted unit leaves copies nobody waits for
+    if (lane == 0) {
+      bool drained = q_last < 0 || mbar_drain(bar(kBarQFull), q_last & 1);
+      for (int s = 0; s < 2; ++s) {
+        if (k_last[s] >= 0) drained &= mbar_drain(bar(kBarKFull + s), (k_last[s] >> 1) & 1);
+        if (v_last[s] >= 0) drained &= mbar_drain(bar(kBarVFull + s), (v_last[s] >> 1) & 1);
+      }
+      if (!drained) set_status(hdr, RPA_STATUS_TIMEOUT);
+    }
   } else if (warp == 1) {
     unit_loop([&](const Geom& g, const uint32_t tcount, const uint32_t ucount) {
       const int nt = g.n_tiles;
@@ -448,6 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     });
+    // every product this thread issued completes before tensor memory is
+    // freed (an aborted unit can leave some in flight)
+    if (lane == 0) {
+      umma_commit(bar(kBarDrain));
+      if (!mbar_drain(bar(kBarDrain), 0)) set_status(hdr, RPA_STATUS_TIMEOUT);
+    }
   } else if (warp < 4) {
     if (FP8) {
       // warps 2 and 3: their shares of the fp8 decoding, tile by tile
