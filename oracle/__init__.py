@@ -17,7 +17,9 @@ follows; the numeric definitions live in ``rpa_oracle.c``:
   ``flash_attention_step1_qk_softmax`` / ``step2_pv`` reach the same value;
   options from the ejkernel ``ragged_page_attention_v3`` interface).
 * ``e4m3_encode`` / ``e4m3_decode`` / ``quantize`` -- the fp8 KV format
-  (tpu-inference 0.11.1rc3 layers/vllm/attention.py, ``quantize_kv``).
+  (tpu-inference 0.11.1rc3 layers/vllm/attention.py, ``quantize_kv``);
+  with ``q_scale`` the queries are quantised the same way (w8a8: the
+  ejkernel interface's ``q_scale``).
 """
 from __future__ import annotations
 
@@ -53,6 +55,7 @@ class OracleParams(ctypes.Structure):
         ("v_scale", ctypes.c_double),
         ("k_scale_heads", ctypes.POINTER(ctypes.c_double)),
         ("v_scale_heads", ctypes.POINTER(ctypes.c_double)),
+        ("q_scale", ctypes.c_double),
     ]
 
 
@@ -121,9 +124,11 @@ def max_threads() -> int:
 def make_params(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                 pages_per_seq, max_num_seqs, total_tokens, kv_fp8=False,
                 sliding_window=0, softmax_scale=1.0, logits_soft_cap=0.0,
-                k_scale=1.0, v_scale=1.0, k_scale_heads=None, v_scale_heads=None) -> OracleParams:
+                k_scale=1.0, v_scale=1.0, k_scale_heads=None, v_scale_heads=None,
+                q_scale=None) -> OracleParams:
     """Scales are fp32 numbers in the interface; they are rounded to fp32 here.
-    ``k_scale_heads`` / ``v_scale_heads``: optional per-kv-head scales (fp8)."""
+    ``k_scale_heads`` / ``v_scale_heads``: optional per-kv-head scales (fp8).
+    ``q_scale``: fp8 only, quantises the queries (None or 0 = off)."""
     f32 = lambda x: float(np.float32(x))
 
     def heads(x):
@@ -141,7 +146,8 @@ def make_params(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                      int(page_size), int(num_pages), int(pages_per_seq),
                      int(max_num_seqs), int(total_tokens), int(bool(kv_fp8)),
                      int(sliding_window or 0), f32(softmax_scale),
-                     f32(logits_soft_cap or 0.0), f32(k_scale), f32(v_scale), kp, vp)
+                     f32(logits_soft_cap or 0.0), f32(k_scale), f32(v_scale), kp, vp,
+                     f32(q_scale or 0.0))
     p._keep = (kh, vh)  # the arrays must live as long as the params
     return p
 

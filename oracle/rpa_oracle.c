@@ -39,6 +39,13 @@
  *     v_scale).  The online-softmax recurrence of the RPA v3 kernel
  *     (flash_attention_step1_qk_softmax / step2_pv) reaches this same value
  *     up to rounding, so the oracle writes the two-pass definition out.
+ *
+ *   - q_scale (fp8 caches, optional: w8a8 attention, the ejkernel
+ *     interface's q_scale, left disabled by tpu-inference 0.11.1rc3
+ *     layers/vllm/attention.py): when q_scale > 0 every query element is
+ *     quantised exactly as keys are (x / q_scale in fp32, E4M3 round to
+ *     nearest even, saturating) and read back as code * q_scale, so the
+ *     logit is softmax_scale * q_scale * k_scale * (q_codes . k_codes).
  */
 #include <math.h>
 #include <stdint.h>
@@ -66,6 +73,7 @@ typedef struct {
   double v_scale;
   const double* k_scale_heads;  /* fp8 only, optional: [num_kv_heads] scales  */
   const double* v_scale_heads;  /* that replace k_scale / v_scale per head   */
+  double q_scale;               /* fp8 only: > 0 quantises the queries; 0 = off */
 } oracle_params;
 
 /* The key / value scale of kv head h. */
@@ -153,6 +161,7 @@ static int check_params(const oracle_params* p) {
   if (p->kv_fp8 && (!(p->k_scale > 0.0) || !(p->v_scale > 0.0)))
     return ORACLE_BAD_ARG;
   if (!p->kv_fp8 && (p->k_scale_heads || p->v_scale_heads)) return ORACLE_BAD_ARG;
+  if (!(p->q_scale >= 0.0) || (p->q_scale > 0.0 && !p->kv_fp8)) return ORACLE_BAD_ARG;
   for (int h = 0; h < p->num_kv_heads; ++h)
     if (!(key_scale(p, h) > 0.0) || !(value_scale(p, h) > 0.0)) return ORACLE_BAD_ARG;
   return ORACLE_OK;
@@ -294,13 +303,14 @@ int oracle_attention_rows(const oracle_params* p, const uint16_t* queries,
 #pragma omp parallel
   {
     double* scores = (double*)malloc(sizeof(double) * (size_t)max_kv);
-    if (!scores) {
+    double* qv = (double*)malloc(sizeof(double) * (size_t)D);  /* the query's values */
+    if (!scores || !qv) {
 #pragma omp atomic write
       failed = 1;
     }
 #pragma omp for schedule(dynamic, 4)
     for (int64_t w = 0; w < (int64_t)num_rows * Hq; ++w) {
-      if (!scores) continue;
+      if (!scores || !qv) continue;
       int r = (int)(w / Hq), hq = (int)(w % Hq);
       int32_t t = tokens[r];
       int s = 0;  /* the sequence whose query range holds token t */
@@ -313,6 +323,13 @@ int oracle_attention_rows(const oracle_params* p, const uint16_t* queries,
       if (p->sliding_window > 0 && pos - p->sliding_window + 1 > 0)
         lo = pos - p->sliding_window + 1;
       const uint16_t* q = queries + ((int64_t)t * Hq + hq) * D;
+      /* the query as the scores see it: bf16 values, or with q_scale the
+       * e4m3 codes of q / q_scale read back as code * q_scale */
+      for (int d = 0; d < D; ++d)
+        qv[d] = p->q_scale > 0.0
+                    ? oracle_e4m3_decode(oracle_quantize(q[d], p->q_scale)) *
+                          (double)(float)p->q_scale
+                    : oracle_bf16_to_double(q[d]);
 
       /* pass 1: logits and their maximum */
       double m = -INFINITY;
@@ -321,8 +338,7 @@ int oracle_attention_rows(const oracle_params* p, const uint16_t* queries,
                                    j % p->page_size, 2 * h);
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
-          dot += oracle_bf16_to_double(q[d]) *
-                 cache_value(p, kv_cache, off, d, key_scale(p, h));
+          dot += qv[d] * cache_value(p, kv_cache, off, d, key_scale(p, h));
         double sc = p->softmax_scale * dot;
         if (p->logits_soft_cap > 0.0)
           sc = p->logits_soft_cap * tanh(sc / p->logits_soft_cap);
@@ -349,6 +365,7 @@ int oracle_attention_rows(const oracle_params* p, const uint16_t* queries,
       for (int d = 0; d < D; ++d) o[d] /= den;
     }
     free(scores);
+    free(qv);
   }
   return failed ? ORACLE_BAD_ARG : ORACLE_OK;
 }

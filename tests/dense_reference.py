@@ -5,7 +5,8 @@ values back out of the pool through the flat slot index
 ``slot = block_tables[s][pos // P] * P + pos % P`` (the slot_mapping
 arithmetic of vLLM 0.10.2 differential_flash_attn.py's metadata builder),
 takes the new tokens from the inputs (quantised through torch's own
-float8_e4m3fn cast for fp8 caches), and evaluates
+float8_e4m3fn cast for fp8 caches, and the queries too when q_scale is
+set), and evaluates
 ``softmax(scale * Q K^T + mask) V`` as whole numpy matrices in fp64 with a
 dense causal/window mask and an extra sink column.
 """
@@ -96,7 +97,10 @@ def dense_attention(w, queries, keys, values, pool_before, sink=None) -> np.ndar
         allowed = j <= pos
         if w.sliding_window:
             allowed &= (pos - j) < w.sliding_window
-        Q = queries[q0:q1].to(torch.float64).numpy()
+        if getattr(w, "q_scale", 0.0):
+            Q = fp8_roundtrip(queries[q0:q1], w.q_scale)
+        else:
+            Q = queries[q0:q1].to(torch.float64).numpy()
         for hq in range(w.num_q_heads):
             h = hq // g
             S = sc * (Q[:, hq, :] @ K[:, h, :].T)

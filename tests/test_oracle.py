@@ -128,6 +128,16 @@ SMALL_CASES = [
                             num_kv_heads=2, logits_soft_cap=50.0, sliding_window=8)),
     ("d96_fp8", lambda: _small("i", 20, [1, 5], [17, 5], head_dim=96, kv_dtype="fp8",
                                k_scale=0.05, v_scale=0.07)),
+    # q_scale: the queries quantised to e4m3 too (the dense reference uses
+    # torch's own float8_e4m3fn cast of q / q_scale)
+    ("fp8_q_scale_all", lambda: _small("j", 21, [1, 9, 4], [31, 17, 4], kv_dtype="fp8",
+                                       k_scale=0.05, v_scale=0.08, q_scale=0.03,
+                                       logits_soft_cap=30.0, has_sink=True, sliding_window=5,
+                                       num_q_heads=8, num_kv_heads=2, page_size=4)),
+    ("fp8_q_scale_per_head_d256", lambda: _small("k", 22, [1, 6, 2], [23, 6, 9], head_dim=256,
+                                                 kv_dtype="fp8", q_scale=0.011,
+                                                 k_scale_heads=[0.04, 0.1],
+                                                 v_scale_heads=[0.06, 0.02])),
 ]
 
 
@@ -390,7 +400,8 @@ def test_equal_per_head_scales_are_the_scalar_scales():
 # ------------------------------------------------------------ random sweep
 def _random_case(i):
     """A seeded random small call: shapes, ragged lengths (some q_len = 0),
-    every option on or off, fp8 with scalar or per-head scales."""
+    every option on or off, fp8 with scalar or per-head scales and with or
+    without quantised queries."""
     rng = np.random.default_rng(1000 + i)
     Hkv = int(rng.integers(1, 4))
     G = int(rng.choice([1, 2, 4]))
@@ -412,6 +423,8 @@ def _random_case(i):
             kw["v_scale_heads"] = [float(x) for x in rng.uniform(0.01, 0.3, Hkv)]
         else:
             kw["k_scale"], kw["v_scale"] = float(rng.uniform(0.02, 0.2)), float(rng.uniform(0.02, 0.2))
+        if rng.integers(0, 2):
+            kw["q_scale"] = float(rng.uniform(0.005, 0.05))
     # decode class: a prefix of the one-token sequences
     d0 = 0
     while d0 < S and q_lens[d0] == 1:
@@ -494,3 +507,60 @@ def test_tolerance_rule_is_the_stated_bound_where_attainable():
     y_got[0] += 0.011
     with pytest.raises(AssertionError):
         assert_close(y_got, y, "one element off by 0.011")
+
+
+# --------------------------------------------------------------- q_scale
+def _q_scale_case(q_scale, **kw):
+    base = dict(num_q_heads=8, num_kv_heads=2, head_dim=16, page_size=4, kv_dtype="fp8",
+                k_scale=0.05, v_scale=0.07, has_sink=True, logits_soft_cap=20.0)
+    base.update(kw)
+    return wl.make_custom("qs", 23, [1, 7, 3], [25, 12, 3], q_scale=q_scale, **base)
+
+
+def test_q_scale_exact_codes_equal_plain_queries():
+    """Queries that are e4m3 values times a power-of-two q_scale quantise
+    exactly, so the w8a8 path must give the plain path's outputs bit for
+    bit (a dropped or doubled q_scale, or quantising with another scale,
+    changes them)."""
+    w8 = _q_scale_case(2.0 ** -4)
+    plain = _q_scale_case(0.0)
+    q, k, v, pool, sink = _inputs(plain)
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 0x7F, size=q.numel()).astype(np.uint8)  # finite, positive
+    codes |= (rng.integers(0, 2, size=q.numel()) << 7).astype(np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float() * 2.0 ** -4
+    qx = vals.reshape(q.shape).to(torch.bfloat16)
+    assert torch.equal(qx.float(), vals.reshape(q.shape))  # exact in bf16
+    o8, c8 = run_oracle(w8, qx, k, v, pool, sink)
+    op, cp = run_oracle(plain, qx, k, v, pool, sink)
+    assert np.array_equal(o8, op) and np.array_equal(c8, cp)
+    # and with another q_scale the same queries do change the outputs
+    o9, _ = run_oracle(_q_scale_case(0.3), qx, k, v, pool, sink)
+    assert not np.array_equal(o9, op)
+
+
+def test_q_scale_saturates_queries():
+    """|q| / q_scale beyond 448 saturates to the largest code: equal to the
+    plain path on queries clamped to +-448 * q_scale."""
+    qs = 2.0 ** -6
+    w8 = _q_scale_case(qs)
+    plain = _q_scale_case(0.0)
+    q, k, v, pool, sink = _inputs(plain)
+    big = (q.float() * 40.0).to(torch.bfloat16)            # |q| up to ~160 >> 448 * 2^-6 = 7
+    clamped = big.float().clamp(-448 * qs, 448 * qs)
+    # inside the range the codes must be exact too: keep the clamped values
+    # and the in-range ones on e4m3 points by snapping through torch's cast
+    snapped = (clamped / qs).to(torch.float8_e4m3fn).float() * qs
+    o8, _ = run_oracle(w8, big, k, v, pool, sink)
+    op, _ = run_oracle(plain, snapped.to(torch.bfloat16), k, v, pool, sink)
+    assert np.max(np.abs(o8 - op)) < 1e-12
+    assert (big.float().abs() > 448 * qs).any()
+
+
+def test_q_scale_needs_an_fp8_cache():
+    w = _small("qb", 24, [1, 3], [9, 3])
+    p = oracle.make_params(**w.params(), q_scale=0.05)
+    q, k, v, pool, sink = _inputs(w)
+    with pytest.raises(oracle.OracleError):
+        oracle.forward(p, q, k, v, pool_bytes(pool), w.kv_lens, w.block_tables,
+                       w.query_start_loc, w.num_seqs)

@@ -70,6 +70,8 @@ class Workload:
     # replace k_scale / v_scale head by head
     k_scale_heads: Optional[np.ndarray] = None
     v_scale_heads: Optional[np.ndarray] = None
+    # fp8 caches: > 0 quantises the queries to e4m3 with this scale (w8a8)
+    q_scale: float = 0.0
 
     # ------------------------------------------------------------- metadata
     @property
@@ -123,7 +125,8 @@ class Workload:
                     logits_soft_cap=self.logits_soft_cap,
                     k_scale=self.k_scale, v_scale=self.v_scale,
                     **({} if self.k_scale_heads is None else {"k_scale_heads": self.k_scale_heads}),
-                    **({} if self.v_scale_heads is None else {"v_scale_heads": self.v_scale_heads}))
+                    **({} if self.v_scale_heads is None else {"v_scale_heads": self.v_scale_heads}),
+                    **({} if not self.q_scale else {"q_scale": self.q_scale}))
 
     # --------------------------------------------------------------- tensors
     def _gen(self, stream: int) -> torch.Generator:
@@ -237,7 +240,7 @@ def make_custom(name: str, seed: int, q_lens, kv_lens, *, num_q_heads, num_kv_he
                 max_num_seqs=None, kv_dtype="bf16", softmax_scale=None,
                 sliding_window=0, logits_soft_cap=0.0, k_scale=1.0, v_scale=1.0,
                 has_sink=False, distribution=None, extra_tokens=0, k_scale_heads=None,
-                v_scale_heads=None) -> Workload:
+                v_scale_heads=None, q_scale=0.0) -> Workload:
     """A workload from explicit per-sequence (q_len, kv_len) lists."""
     q_lens = np.asarray(q_lens, dtype=np.int32)
     kv_lens = np.asarray(kv_lens, dtype=np.int32)
@@ -271,7 +274,8 @@ def make_custom(name: str, seed: int, q_lens, kv_lens, *, num_q_heads, num_kv_he
                     k_scale_heads=None if k_scale_heads is None
                     else np.asarray(k_scale_heads, np.float32),
                     v_scale_heads=None if v_scale_heads is None
-                    else np.asarray(v_scale_heads, np.float32))
+                    else np.asarray(v_scale_heads, np.float32),
+                    q_scale=float(q_scale or 0.0))
 
 
 def _randint(g, lo, hi, n):
