@@ -316,7 +316,7 @@ def prepare(w, dev):
         "pool": w.make_pool(dev),
         "kw": dict(softmax_scale=w.softmax_scale, sliding_window=w.sliding_window,
                    logits_soft_cap=w.logits_soft_cap, k_scale=w.k_scale if fp8 else None,
-                   v_scale=w.v_scale if fp8 else None),
+                   v_scale=w.v_scale if fp8 else None, q_scale=w.q_scale or None),
     }
     ctx["out"] = torch.empty_like(ctx["dev"][0])
     ctx["ws"] = rpa.alloc_workspace(rpa.make_params(**w.params()), dev)

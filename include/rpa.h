@@ -79,8 +79,8 @@ extern "C" {
 /* Return codes of every entry point. */
 #define RPA_OK 0
 #define RPA_ERR_INVALID_ARG 1  /* null or misaligned pointer, negative size,
-                                  bad scale, per-head scales with a bf16
-                                  cache                                    */
+                                  bad scale, per-head scales or q_scale
+                                  with a bf16 cache                        */
 #define RPA_ERR_UNSUPPORTED 2  /* head_dim not 64/96/128/192/256, Hq/Hkv not in {1,2,4,8,16},
                                   page_size not a power of two in [1,1024],
                                   or an fp8 cache with head_dim 64/96 and
@@ -125,6 +125,14 @@ typedef struct {
    * per kv head is the finer variant.) */
   const float* k_scale_heads;
   const float* v_scale_heads;
+  /* fp8 caches only, optional (w8a8 attention; the ejkernel
+   * ragged_page_attention_v3 interface's q_scale): when > 0, every query
+   * element is quantised exactly as the keys are -- x / q_scale in fp32,
+   * e4m3 with round to nearest even, saturating at +-448 -- and the scores
+   * are formed from the codes: logit = softmax_scale * q_scale * k_scale *
+   * (q_codes . k_codes).  0 = the queries are used as given (bf16).  Must be
+   * finite and >= 0; > 0 with a bf16 cache is refused (RPA_ERR_INVALID_ARG). */
+  float q_scale;
 } rpa_params_t;
 
 /* Bytes of device workspace rpa_forward / rpa_update_cache need for these

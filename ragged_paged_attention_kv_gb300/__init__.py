@@ -9,10 +9,11 @@ fallback.
     out = forward(queries, keys, values, kv_cache, kv_lens, block_tables,
                   query_start_loc, distribution, attention_sink=None,
                   softmax_scale=..., sliding_window=None, logits_soft_cap=None,
-                  k_scale=None, v_scale=None)
+                  k_scale=None, v_scale=None, q_scale=None)
 
 ``k_scale`` / ``v_scale`` are numbers, or (fp8 caches) float32 device tensors
-of num_kv_heads entries for one scale per kv head.  The argument list follows the ejkernel ``ragged_page_attention_v3``
+of num_kv_heads entries for one scale per kv head; ``q_scale`` (fp8 caches)
+quantises the queries to e4m3 as well (w8a8).  The argument list follows the ejkernel ``ragged_page_attention_v3``
 interface; ``kv_cache`` is updated in place (the new keys/values are written
 into their pages) instead of being returned.
 """
@@ -33,10 +34,11 @@ __all__ = ["make_params", "workspace_size", "alloc_workspace", "forward", "updat
 def make_params(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, pages_per_seq,
                 max_num_seqs, total_tokens, kv_fp8=False, sliding_window=None,
                 softmax_scale=1.0, logits_soft_cap=None, k_scale=None, v_scale=None,
-                k_scale_heads=None, v_scale_heads=None) -> RpaParams:
+                k_scale_heads=None, v_scale_heads=None, q_scale=None) -> RpaParams:
     """``k_scale_heads`` / ``v_scale_heads``: optional float32 device tensors of
     num_kv_heads per-head scales (fp8 caches); they must outlive the calls
-    that use these params."""
+    that use these params.  ``q_scale`` (fp8 caches): quantise the queries to
+    e4m3 with this scale (None or 0 = off)."""
     return RpaParams(int(num_q_heads), int(num_kv_heads), int(head_dim), int(page_size),
                      int(num_pages), int(pages_per_seq), int(max_num_seqs), int(total_tokens),
                      _lib.RPA_KV_FP8_E4M3 if kv_fp8 else _lib.RPA_KV_BF16,
@@ -44,7 +46,8 @@ def make_params(*, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, pa
                      float(1.0 if k_scale is None else k_scale),
                      float(1.0 if v_scale is None else v_scale),
                      None if k_scale_heads is None else k_scale_heads.data_ptr(),
-                     None if v_scale_heads is None else v_scale_heads.data_ptr())
+                     None if v_scale_heads is None else v_scale_heads.data_ptr(),
+                     float(q_scale or 0.0))
 
 
 def workspace_size(params: RpaParams) -> int:
@@ -93,7 +96,8 @@ def _scale_arg(x, name, Hkv, device):
 
 
 def _params_from(queries_or_none, keys, kv_cache, kv_lens, block_tables, softmax_scale,
-                 sliding_window, logits_soft_cap, k_scale, v_scale, num_q_heads=None):
+                 sliding_window, logits_soft_cap, k_scale, v_scale, num_q_heads=None,
+                 q_scale=None):
     T, Hkv, D = keys.shape
     k_scale, k_heads = _scale_arg(k_scale, "k_scale", Hkv, keys.device)
     v_scale, v_heads = _scale_arg(v_scale, "v_scale", Hkv, keys.device)
@@ -110,13 +114,13 @@ def _params_from(queries_or_none, keys, kv_cache, kv_lens, block_tables, softmax
                        max_num_seqs=max_num_seqs, total_tokens=T, kv_fp8=fp8,
                        sliding_window=sliding_window, softmax_scale=softmax_scale,
                        logits_soft_cap=logits_soft_cap, k_scale=k_scale, v_scale=v_scale,
-                       k_scale_heads=k_heads, v_scale_heads=v_heads)
+                       k_scale_heads=k_heads, v_scale_heads=v_heads, q_scale=q_scale)
 
 
 def forward(queries, keys, values, kv_cache, kv_lens, block_tables, query_start_loc,
             distribution, attention_sink=None, *, softmax_scale=1.0, sliding_window=None,
-            logits_soft_cap=None, k_scale=None, v_scale=None, out=None, workspace=None,
-            stream=None, events=None) -> torch.Tensor:
+            logits_soft_cap=None, k_scale=None, v_scale=None, q_scale=None, out=None,
+            workspace=None, stream=None, events=None) -> torch.Tensor:
     """Writes the new keys/values into ``kv_cache`` and returns the attention
     output [total_tokens, num_q_heads, head_dim] (bf16).  Asynchronous on the
     current (or given) stream; data-dependent problems are reported through
@@ -139,7 +143,7 @@ def forward(queries, keys, values, kv_cache, kv_lens, block_tables, query_start_
     if query_start_loc.numel() != kv_lens.numel() + 1 or distribution.numel() != 3:
         raise ValueError("query_start_loc must have max_num_seqs+1 entries, distribution 3")
     params = _params_from(queries, keys, kv_cache, kv_lens, block_tables, softmax_scale,
-                          sliding_window, logits_soft_cap, k_scale, v_scale)
+                          sliding_window, logits_soft_cap, k_scale, v_scale, q_scale=q_scale)
     if attention_sink is not None and attention_sink.numel() != params.num_q_heads:
         raise ValueError("attention_sink must have num_q_heads entries")
     if out is None:

@@ -54,6 +54,7 @@ class RpaParams(ctypes.Structure):
         ("v_scale", ctypes.c_float),
         ("k_scale_heads", ctypes.c_void_p),
         ("v_scale_heads", ctypes.c_void_p),
+        ("q_scale", ctypes.c_float),
     ]
 
 

@@ -2,6 +2,7 @@
 // sizing and the launch sequence plan -> decode -> prefill on the caller's
 // stream.  No entry point allocates device memory or synchronises (except
 // rpa_get_status).
+#include <cfloat>
 #include <cstring>
 
 #include "common.cuh"
@@ -33,6 +34,9 @@ static int check_params(const rpa_params_t* p) {
       p->page_size < 2)
     return RPA_ERR_UNSUPPORTED;
   if (!(p->softmax_scale > 0.f) || !(p->logits_soft_cap >= 0.f))
+    return RPA_ERR_INVALID_ARG;
+  if (!(p->q_scale >= 0.f) || !(p->q_scale <= FLT_MAX) ||
+      (p->q_scale > 0.f && p->kv_dtype != RPA_KV_FP8_E4M3))
     return RPA_ERR_INVALID_ARG;
   if (p->kv_dtype == RPA_KV_FP8_E4M3) {
     if (!(p->k_scale > 0.f) || !(p->v_scale > 0.f)) return RPA_ERR_INVALID_ARG;

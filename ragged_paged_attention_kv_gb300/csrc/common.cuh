@@ -339,6 +339,17 @@ struct LogitXform {
     return dot * mul;
   }
 };
+// The factor the raw q . k dot product carries besides softmax_scale: the
+// key scale, times q_scale when the queries are quantised (the dot product
+// is then one of e4m3 codes).
+__device__ __forceinline__ float qk_scale(const rpa_params_t& p, float k_scale) {
+  return p.q_scale > 0.f ? k_scale * p.q_scale : k_scale;
+}
+// Quantises 8 queries (one 16-byte chunk, in place) to e4m3 with q_scale and
+// back to bf16 (exact): the operand then holds the codes' values.
+__device__ __forceinline__ void quantize_q8(uint4* chunk, float q_scale) {
+  *chunk = dequant8(quantize8(*chunk, q_scale));
+}
 __device__ __forceinline__ LogitXform make_xform(float softmax_scale, float k_scale, float cap) {
   return cap > 0.f ? LogitXform{softmax_scale * k_scale / cap, cap * kLog2e}
                    : LogitXform{softmax_scale * k_scale * kLog2e, 0.f};

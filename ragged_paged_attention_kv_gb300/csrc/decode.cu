@@ -295,6 +295,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
     // the consumer warps leave together or not at all: a warp that left
     // alone would leave the others at the next named barrier
     const bool q_ok = mbar_wait(bar_qfull + 8 * slot, (uq >> 1) & 1, &s_abort);
+    if (FP8 && q_ok && p.q_scale > 0.f) {  // q_scale needs an e4m3 cache
+      // quantised queries: the slot's rows become their e4m3 codes' values
+      // before any warp reads them (the vote below is a barrier)
+      uint8_t* qslot = smem + C::kOffQ + slot * C::kQBytes;
+      for (int idx = tid; idx < G * (D / 8); idx += kConsumerWarps * 32)
+        quantize_q8(reinterpret_cast<uint4*>(qslot + (idx / (D / 8)) * C::kQRow +
+                                             (idx % (D / 8)) * 16),
+                    p.q_scale);
+    }
     if (!named_bar_all(1, kConsumerWarps * 32, q_ok)) {
       if (!q_ok && lane == 0) set_status(hdr, RPA_STATUS_TIMEOUT);
       s_abort = 1;
@@ -307,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
     const int q0 = info[slot].q0;
     const int ctx = info[slot].ctx;
     const float ks = k_scale_of(p, h), vs = v_scale_of(p, h);  // this kv head's scales
-    const LogitXform xf = make_xform(p.softmax_scale, ks, p.logits_soft_cap);
+    const LogitXform xf = make_xform(p.softmax_scale, qk_scale(p, ks), p.logits_soft_cap);
     // split 0 stores the new token's key/value into its page after the
     // stages; the page id and the inputs are loaded now so that store does
     // not wait for them

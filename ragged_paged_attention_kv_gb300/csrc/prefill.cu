@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
     const PrefillUnit pu = units[u];
     const int seq = pu.seq, h = pu.head;
     const float ks = k_scale_of(p, h);  // this kv head's key scale
-    const LogitXform xf = make_xform(p.softmax_scale, ks, p.logits_soft_cap);
+    const LogitXform xf = make_xform(p.softmax_scale, qk_scale(p, ks), p.logits_soft_cap);
     const int q0 = a.qsl[seq];
     const int q_len = a.qsl[seq + 1] - q0;
     const int ctx = a.kv_lens[seq] - q_len;
@@ -170,6 +170,12 @@ __global__ void __launch_bounds__(kThreads) prefill_kernel(AttnArgs a) {
       cp_async_commit();
       cp_async_wait<1>();
       __syncthreads();
+      if (FP8 && kt == 0 && p.q_scale > 0.f) {  // q_scale needs an e4m3 cache
+        // quantised queries: the tile becomes its e4m3 codes' values
+        for (int i = tid; i < S::kQBytes / 16; i += kThreads)
+          quantize_q8(reinterpret_cast<uint4*>(sQ) + i, p.q_scale);
+        __syncthreads();
+      }
       if constexpr (!kQFromSmem) {
         if (kt == 0) {
 #pragma unroll

@@ -92,7 +92,8 @@ enum Bar {
   kBarPReady = 15,  // [2] per query tile: P written (and O corrected)
   kBarODone = 17,   // [2] per query tile: the unit's last PV product done
   kBarDrain = 19,   // once, at exit: every tcgen05 product the MMA thread issued is done
-  kNumBars = 20,
+  kBarQReady = 20,  // quantised queries (q_scale): the softmax warps converted the tiles
+  kNumBars = 21,
 };
 
 struct TcMaps {
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarODone + s), 1);
     }
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarQReady), 8);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t idesc_pv = idesc_bf16(kM, D, false, true, FP8);
   const bool has_cap = p.logits_soft_cap > 0.f;
   // the logit transform of the scalar key scale (used unless per-head scales)
-  const LogitXform xf0 = make_xform(p.softmax_scale, p.k_scale, p.logits_soft_cap);
+  const LogitXform xf0 = make_xform(p.softmax_scale, qk_scale(p, p.k_scale), p.logits_soft_cap);
 
   // Every role runs this loop over the CTA's units with its own body, so
   // the code of each role stays within its register budget; all threads meet
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // the last query copy (unit count) and the last key / value copy (tile
       // count) per stage this warp issued, for the drain at exit
-      int q_last = -1, k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
+      int q_last = -1, k_last0 = -1, k_last1 = -1, v_last0 = -1, v_last1 = -1;
       unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t ucount) {
       const int nt = g.n_tiles;
       // ------------------------------------------------------- TMA producer
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         issue(j, 0, tc, ids);
-        k_last[s] = (int)tc;
+        (s ? k_last1 : k_last0) = (int)tc;
         if (FP8 && !kStg1 && j >= 1) {
           ok = finalize_k(tc - 1, j - 1);
           if (!ok) break;
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         issue(j, 1, tc, ids);
-        v_last[s] = (int)tc;
+        (s ? v_last1 : v_last0) = (int)tc;
         __syncwarp();
         if (!kStg1 && j >= 1) ok = finalize_v(tc - 1, j - 1);
       }
@@ -446,9 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // memory: an aborted unit leaves copies nobody waits for
       if (lane == 0) {
         bool drained = q_last < 0 || mbar_drain(bar(kBarQFull), q_last & 1);
+        const int kl[2] = {k_last0, k_last1}, vl[2] = {v_last0, v_last1};
         for (int s = 0; s < 2; ++s) {
-          if (k_last[s] >= 0) drained &= mbar_drain(bar(kBarKFull + s), (k_last[s] >> 1) & 1);
-          if (v_last[s] >= 0) drained &= mbar_drain(bar(kBarVFull + s), (v_last[s] >> 1) & 1);
+          if (kl[s] >= 0) drained &= mbar_drain(bar(kBarKFull + s), (kl[s] >> 1) & 1);
+          if (vl[s] >= 0) drained &= mbar_drain(bar(kBarVFull + s), (vl[s] >> 1) & 1);
         }
         if (!drained) set_status(hdr, RPA_STATUS_TIMEOUT);
       }
@@ -463,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and its completion also tells the softmax of tile X that PV_X(j) is
       // done, so O_X may be rescaled.
       if (lane == 0) {
-        bool ok = mbar_wait(bar(kBarQFull), ucount & 1, &s_abort);
+        bool ok = mbar_wait(bar(FP8 && p.q_scale > 0.f ? kBarQReady : kBarQFull), ucount & 1,
+                            &s_abort);
         tc_fence_after();
         auto qk = [&](uint32_t tc, int x, bool last_of_stage) -> bool {
           const int s = tc & 1;
@@ -555,7 +559,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = g.n_tiles;
     // tile B holds tokens t_begin + 128/G onwards; it may be empty
     const bool has_b = g.t_begin + kM / G < g.t_end;
-    if (warp < 8 || has_b) {
+    bool q_ok = true;
+    if (FP8 && p.q_scale > 0.f) {  // q_scale needs an e4m3 cache
+      // quantised queries: all eight softmax warps turn both query tiles
+      // into their e4m3 codes' values (element by element, in place) before
+      // the MMA thread reads them
+      q_ok = mbar_wait(bar(kBarQFull), ucount & 1, &s_abort);
+      if (q_ok) {
+        uint4* qt = reinterpret_cast<uint4*>(smem + kOffQ);
+        for (int i = tid - 128; i < (int)(2 * kOperand / 16); i += 256) quantize_q8(qt + i, p.q_scale);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQReady));
+      } else if (lane == 0) {
+        set_status(hdr, RPA_STATUS_TIMEOUT);
+        s_abort = 1;
+      }
+    }
+    if (q_ok && (warp < 8 || has_b)) {
       // ---------------------------------------------- softmax of tile x
       const int x = (warp - 4) >> 2;           // query tile of this warpgroup
       const int q4 = warp & 3;                 // tensor-memory lane quarter
@@ -596,7 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // plain load of this head's scale (reissued after every barrier wait)
         // rather than held in registers across the tile loop
         const LogitXform xf =
-            PH ? make_xform(p.softmax_scale, p.k_scale_heads ? p.k_scale_heads[g.h] : p.k_scale,
+            PH ? make_xform(p.softmax_scale,
+                            qk_scale(p, p.k_scale_heads ? p.k_scale_heads[g.h] : p.k_scale),
                             p.logits_soft_cap)
                : xf0;
         const float sc = has_cap ? 1.f : xf.mul;  // raw score -> log2-domain logit

@@ -81,7 +81,8 @@ enum Bar {
   kBarPVDone = 17,  // every P V product done, in order (for O rescales)
   kBarODone = 18,   // the unit's last P V product done
   kBarDrain = 19,   // once, at exit: every tcgen05 product the MMA thread issued is done
-  kNumBars = 20,
+  kBarQReady = 20,  // quantised queries (q_scale): the softmax warps converted the tile
+  kNumBars = 21,
 };
 
 struct Maps {
@@ -182,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarPVDone), 1);
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarQReady), 4);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // P and the values are fp16 with an e4m3 cache, bf16 otherwise
   const uint32_t idesc_pv = idesc_bf16(kM, D, false, true, FP8);
   const bool has_cap = p.logits_soft_cap > 0.f;
-  const LogitXform xf0 = make_xform(p.softmax_scale, p.k_scale, p.logits_soft_cap);
+  const LogitXform xf0 = make_xform(p.softmax_scale, qk_scale(p, p.k_scale), p.logits_soft_cap);
 
   // fp8 cache: decoding of a landed operand of tile j (staged codes, or for
   // new rows the bf16 inputs quantised in place so they carry the codes the
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // the last query copy (unit count) and the last key / value copy (tile
     // count) per stage this warp issued, for the drain at exit
-    int q_last = -1, k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
+    int q_last = -1, k_last0 = -1, k_last1 = -1, v_last0 = -1, v_last1 = -1;
     unit_loop([&](const Geom& g, const uint32_t tcount, const uint32_t ucount) {
       const int nt = g.n_tiles;
       // ----------------------------------------------------- TMA producer
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         issue(j, 0, tc, ids);
-        k_last[s] = (int)tc;
+        (s ? k_last1 : k_last0) = (int)tc;
         if (FP8 && j >= 1) {
           ok = finalize_v(tc - 1, j - 1) &&
                mbar_wait(bar(kBarVReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         issue(j, 1, tc, ids);
-        v_last[s] = (int)tc;
+        (s ? v_last1 : v_last0) = (int)tc;
         __syncwarp();
         if (!FP8 && j >= 1) ok = finalize_v(tc - 1, j - 1);
       }
@@ -407,9 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // memory: an aborted unit leaves copies nobody waits for
     if (lane == 0) {
       bool drained = q_last < 0 || mbar_drain(bar(kBarQFull), q_last & 1);
+      const int kl[2] = {k_last0, k_last1}, vl[2] = {v_last0, v_last1};
       for (int s = 0; s < 2; ++s) {
-        if (k_last[s] >= 0) drained &= mbar_drain(bar(kBarKFull + s), (k_last[s] >> 1) & 1);
-        if (v_last[s] >= 0) drained &= mbar_drain(bar(kBarVFull + s), (v_last[s] >> 1) & 1);
+        if (kl[s] >= 0) drained &= mbar_drain(bar(kBarKFull + s), (kl[s] >> 1) & 1);
+        if (vl[s] >= 0) drained &= mbar_drain(bar(kBarVFull + s), (vl[s] >> 1) & 1);
       }
       if (!drained) set_status(hdr, RPA_STATUS_TIMEOUT);
     }
@@ -420,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S(0), S(1), then per tile j: P V(j), S(j+2).  Key stage and S slot
       // of tile j are both (tcount + j) & 1.
       if (lane == 0) {
-        bool ok = mbar_wait(bar(kBarQFull), ucount & 1, &s_abort);
+        bool ok = mbar_wait(bar(FP8 && p.q_scale > 0.f ? kBarQReady : kBarQFull), ucount & 1,
+                            &s_abort);
         tc_fence_after();
         auto qk = [&](uint32_t tc) -> bool {
           const int s = tc & 1;
@@ -513,6 +517,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = g.ctx + i_tok;
       const int hq = g.h * G + r % G;
       const uint32_t tO = tmem + lane_off + kTmemO;
+      if (FP8 && p.q_scale > 0.f) {  // q_scale needs an e4m3 cache
+        // quantised queries: the four softmax warps turn the query tile into
+        // its e4m3 codes' values (element by element, in place) before the
+        // MMA thread reads it
+        if (!mbar_wait(bar(kBarQFull), ucount & 1, &s_abort)) {
+          if (lane == 0) {
+            set_status(hdr, RPA_STATUS_TIMEOUT);
+            s_abort = 1;
+          }
+          return;
+        }
+        uint4* qt = reinterpret_cast<uint4*>(smem + C::kOffQ);
+        for (int i = tid - 128; i < (int)(C::kQBytes / 16); i += 128) quantize_q8(qt + i, p.q_scale);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQReady));
+      }
 
       // this unit's new tokens -> their pages, a quarter of them per warp
       {
@@ -537,7 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int key0, valid;
         g.tile(j, is_new, key0, valid);
         const LogitXform xf =
-            PH ? make_xform(p.softmax_scale, p.k_scale_heads ? p.k_scale_heads[g.h] : p.k_scale,
+            PH ? make_xform(p.softmax_scale,
+                            qk_scale(p, p.k_scale_heads ? p.k_scale_heads[g.h] : p.k_scale),
                             p.logits_soft_cap)
                : xf0;
         const float sc = has_cap ? 1.f : xf.mul;  // raw score -> log2-domain logit

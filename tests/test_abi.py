@@ -61,6 +61,12 @@ def _params(**over):
     return make_params(**kw)
 
 
+def test_q_scale_accepted_with_an_fp8_cache(lib):
+    n = ctypes.c_size_t(0)
+    p = _params(kv_fp8=True, q_scale=0.05)
+    assert lib.rpa_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0 and n.value > 0
+
+
 def test_workspace_size_host_only(lib):
     from ragged_paged_attention_kv_gb300 import workspace_size
     n = workspace_size(_params())
@@ -92,6 +98,10 @@ def test_supported_head_dims(lib, head_dim):
     (dict(softmax_scale=-0.5), 1),
     (dict(k_scale_heads=_Ptr(256)), 1),           # per-head scales need an fp8 cache
     (dict(kv_fp8=True, v_scale_heads=_Ptr(258)), 1),  # misaligned per-head scales
+    (dict(q_scale=0.05), 1),                      # quantised queries need an fp8 cache
+    (dict(kv_fp8=True, q_scale=-0.05), 1),
+    (dict(kv_fp8=True, q_scale=float("inf")), 1),
+    (dict(kv_fp8=True, q_scale=float("nan")), 1),
 ])
 def test_invalid_params_are_refused(lib, over, code):
     n = ctypes.c_size_t(0)

@@ -51,8 +51,8 @@ def run_gpu(w, q, k, v, pool_before, sink=None, workspace=None, out=None):
                 _dev(w.query_start_loc), _dev(w.distribution),
                 None if sink is None else _dev(sink),
                 softmax_scale=w.softmax_scale, sliding_window=w.sliding_window,
-                logits_soft_cap=w.logits_soft_cap, k_scale=ks, v_scale=vs, out=out_t,
-                workspace=ws)
+                logits_soft_cap=w.logits_soft_cap, k_scale=ks, v_scale=vs, q_scale=w.q_scale,
+                out=out_t, workspace=ws)
     status = rpa.get_status(ws)
     torch.cuda.synchronize()
     return out_t.float().cpu().numpy().astype(np.float64), pool.cpu(), status
@@ -328,6 +328,50 @@ TCW_CASES = [
 
 @pytest.mark.parametrize("name,make", TCW_CASES, ids=[c[0] for c in TCW_CASES])
 def test_tcgen05_wide_prefill_cases(name, make):
+    check_case(make())
+
+
+# Quantised queries (q_scale, w8a8): every kernel path with an e4m3 cache --
+# decode at head_dim 64 / 96 (one bulk copy per query row) / 128 / 256
+# (query fragments re-read from shared memory), the tcgen05 prefill at 64
+# and 128, the head_dim 192/256 tcgen05 prefill, and the warp-level MMA
+# prefill (pages of 4 rows) -- with per-head scales and every option.
+def _q8(name, seed, q_lens, kv_lens, **kw):
+    base = dict(num_q_heads=16, num_kv_heads=4, head_dim=64, page_size=16, kv_dtype="fp8",
+                k_scale=0.05, v_scale=0.07, q_scale=0.02)
+    base.update(kw)
+    return wl.make_custom(name, seed, q_lens, kv_lens, **base)
+
+
+Q8_CASES = [
+    ("decode_d64_options", lambda: _q8("q1", 501, [1] * 5, [900, 129, 5, 2000, 77],
+                                       num_q_heads=64, num_kv_heads=8, logits_soft_cap=30.0,
+                                       has_sink=True, sliding_window=128)),
+    ("decode_d128_per_head_splits", lambda: _q8("q2", 502, [1] * 4, [1400, 70, 3000, 9],
+                                                head_dim=128, k_scale_heads=[0.02, 0.05, 0.11, 0.3],
+                                                v_scale_heads=[0.07, 0.015, 0.2, 0.05])),
+    ("decode_d96", lambda: _q8("q3", 503, [1] * 3, [500, 3, 100], head_dim=96)),
+    ("decode_d256", lambda: _q8("q4", 504, [1] * 3, [700, 17, 1290], head_dim=256,
+                                num_q_heads=16, num_kv_heads=8)),
+    ("tc_prefill_d64_mixed", lambda: _q8("q5", 505, [1, 1, 64, 20], [900, 129, 200, 20],
+                                         num_q_heads=64, num_kv_heads=8, logits_soft_cap=30.0,
+                                         has_sink=True)),
+    ("tc_prefill_d128_tiles", lambda: _q8("q6", 506, [1, 300, 33], [800, 700, 33],
+                                          head_dim=128, num_q_heads=32, num_kv_heads=8,
+                                          sliding_window=300)),
+    ("tcw_prefill_d256_per_head", lambda: _q8("q7", 507, [1, 90, 33], [600, 500, 33],
+                                              head_dim=256, num_q_heads=16, num_kv_heads=2,
+                                              k_scale_heads=[0.04, 0.1],
+                                              v_scale_heads=[0.06, 0.02], has_sink=True)),
+    ("tcw_prefill_d192", lambda: _q8("q8", 508, [1, 70, 8], [900, 200, 8], head_dim=192,
+                                     num_q_heads=8, num_kv_heads=2, logits_soft_cap=20.0)),
+    ("mma_prefill_p4", lambda: _q8("q9", 509, [1, 25, 9], [90, 60, 40], page_size=4,
+                                   sliding_window=20)),
+]
+
+
+@pytest.mark.parametrize("name,make", Q8_CASES, ids=[c[0] for c in Q8_CASES])
+def test_quantised_query_cases(name, make):
     check_case(make())
 
 
