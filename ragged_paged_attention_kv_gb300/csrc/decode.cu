@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
   const int G = p.num_q_heads / p.num_kv_heads;
   const int P = p.page_size;
   griddep_wait();  // the planner's unit list and counters are complete
+  // only now may the prefill kernel behind launch: it reads the planner's
+  // output without a wait of its own
   griddep_launch_dependents();
   if (hdr[kHdrNumDecode] == 0) return;  // a prefill-only batch: nothing to set up
 

@@ -163,9 +163,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.num_q_heads / p.num_kv_heads;
   const int P = p.page_size;
   const int W = p.sliding_window;
-  griddep_wait();  // the planner (and the decode kernel ahead) are complete
-  const int n_units = hdr[kHdrNumPrefill];
-  if (n_units == 0) return;  // a decode-only batch: nothing to set up
+  // No wait on the kernel ahead (the decode kernel) before the work: this
+  // kernel needs nothing it writes, so its CTAs may start on the SMs the
+  // decode tail frees.  The planner's output is complete and visible: every
+  // decode CTA lets this grid launch only after its own wait on the planner
+  // (and a launch starts with a fresh L1).  Every CTA waits for the decode
+  // grid before it exits, so this grid never completes before it: whatever
+  // follows on the stream still finds both kernels done.
+  const int n_units = __ldcg(hdr + kHdrNumPrefill);
+  if (n_units == 0) {  // a decode-only batch: nothing to set up
+    griddep_wait();     // complete only after the decode kernel ahead
+    return;
+  }
 
   if (tid == 0) {
     s_abort = 0;
@@ -676,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  griddep_wait();  // complete only after the decode kernel ahead
 }
 
 }  // namespace tcw
