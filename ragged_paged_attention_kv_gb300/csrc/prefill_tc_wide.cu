@@ -622,38 +622,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float nm = m_run == -INFINITY ? 0.f : -m_run;
         const uint64_t sc2 = f2_pack(sc, sc), nm2 = f2_pack(nm, nm);
-        uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-        // P packed as pairs into sr[0..32) (bf16, or fp16 with an e4m3
-        // cache); the row sums add exactly those rounded weights
+        // P packed as pairs into sr[0..kN/2): bf16, or fp16 with an e4m3 cache
+        // (the values' type).  Scale-and-subtract uses packed f32x2
+        // arithmetic, the exponentials the hardware ex2.
 #pragma unroll
         for (int c = 0; c < kN; c += 2) {
           const uint64_t x2 =
               f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nm2);
           float x0, x1;
           f2_unpack(x2, x0, x1);
-          const uint32_t pk = pack_p<FP8>(fast_exp2(x0), fast_exp2(x1));
-          float r0, r1;
-          if (FP8) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk));
-            r0 = f.x;
-            r1 = f.y;
-          } else {
-            r0 = __uint_as_float(pk << 16);
-            r1 = __uint_as_float(pk & 0xFFFF0000u);
-          }
-          rs2[(c >> 1) & 1] = f2_add(rs2[(c >> 1) & 1], f2_pack(r0, r1));
-          sr[c >> 1] = pk;
-        }
-        {
-          float a0, a1, b0, b1;
-          f2_unpack(rs2[0], a0, a1);
-          f2_unpack(rs2[1], b0, b1);
-          l_run += (a0 + a1) + (b0 + b1);
+          sr[c >> 1] = pack_p<FP8>(fast_exp2(x0), fast_exp2(x1));
         }
         tmem_st32p(tS, sr);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarPReady + s));
+        // the row sum adds exactly the rounded weights just stored; it is
+        // formed after P is handed over, off the tensor core's wait
+        {
+          uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+          for (int c = 0; c < kN / 2; ++c) {
+            const uint32_t pk = sr[c];
+            float r0, r1;
+            if (FP8) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk));
+              r0 = f.x;
+              r1 = f.y;
+            } else {
+              r0 = __uint_as_float(pk << 16);
+              r1 = __uint_as_float(pk & 0xFFFF0000u);
+            }
+            rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(r0, r1));
+          }
+          float a0, a1, b0, b1;
+          f2_unpack(rs2[0], a0, a1);
+          f2_unpack(rs2[1], b0, b1);
+          l_run += (a0 + a1) + (b0 + b1);
+        }
       }
       // epilogue: O / l -> bf16 rows
       if (ok && !mbar_wait(bar(kBarODone), ucount & 1, &s_abort)) ok = false;
