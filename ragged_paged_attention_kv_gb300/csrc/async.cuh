@@ -80,6 +80,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait for a whole warp (all 32 lanes call it): every lane returns from
+// its own bounded wait, then the warp agrees on one outcome.  Lanes that saw
+// the abort flag at different moments would otherwise leave their loop
+// apart, and the warp's next collective (a .sync.aligned tensor-memory load,
+// an ldmatrix / mma.sync, a __syncwarp) would wait for lanes that never come.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
 // Waits for the phase of parity `parity` without looking at the abort flag:
 // an aborting CTA uses it to let the asynchronous copies and tensor-core
 // products it issued finish before it frees their shared or tensor memory

@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
       };
       int ids_next[2] = {0, 0};
       if (n_st > 0) load_ids(0, ids_next);
-      if (!mbar_wait(bar_qempty + 8 * slot, ((uq >> 1) & 1) ^ 1, &s_abort)) {
+      if (!mbar_wait_warp(bar_qempty + 8 * slot, ((uq >> 1) & 1) ^ 1, &s_abort)) {
         ok = false;
         break;
       }
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         int ids[2] = {ids_next[0], ids_next[1]};
         if (st + 1 < n_st) load_ids(st + 1, ids_next);
         const int s = g % C::kStages;
-        if (!mbar_wait(bar_empty + 8 * s, ((g / C::kStages) & 1) ^ 1, &s_abort)) {
+        if (!mbar_wait_warp(bar_empty + 8 * s, ((g / C::kStages) & 1) ^ 1, &s_abort)) {
           ok = false;
           break;
         }
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
     bool ok = true;
     for (int st = 0; st < n_st; ++st, ++g) {
       const int s = g % C::kStages;
-      if (!mbar_wait(bar_full + 8 * s, (g / C::kStages) & 1, &s_abort)) {
+      if (!mbar_wait_warp(bar_full + 8 * s, (g / C::kStages) & 1, &s_abort)) {
         ok = false;
         break;
       }

@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto finalize_k = [&](uint32_t tc, int j) -> bool {
         const int s = tc & 1;
-        if (!mbar_wait(bar(kBarKFull + s), (tc >> 1) & 1, &s_abort)) return false;
+        if (!mbar_wait_warp(bar(kBarKFull + s), (tc >> 1) & 1, &s_abort)) return false;
         decode_fp8(g, tc, j, 0, 0);
         fence_proxy_async();
         __syncwarp();
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto finalize_v = [&](uint32_t tc, int j) -> bool {
         const int s = tc & 1;
-        if (!mbar_wait(bar(kBarVFull + s), (tc >> 1) & 1, &s_abort)) return false;
+        if (!mbar_wait_warp(bar(kBarVFull + s), (tc >> 1) & 1, &s_abort)) return false;
         if (FP8) {
           decode_fp8(g, tc, j, 1, 0);
           fence_proxy_async();
@@ -419,10 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the single staging buffer is refilled once every decoding warp
           // is done with tile j-1's codes
           ok = finalize_k(tc - 1, j - 1) &&
-               mbar_wait(bar(kBarKReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
+               mbar_wait_warp(bar(kBarKReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
           if (!ok) break;
         }
-        if (!mbar_wait(bar(kBarKEmpty + s), par, &s_abort)) {
+        if (!mbar_wait_warp(bar(kBarKEmpty + s), par, &s_abort)) {
           ok = false;
           break;
         }
@@ -434,10 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (kStg1 && j >= 1) {
           ok = finalize_v(tc - 1, j - 1) &&
-               mbar_wait(bar(kBarVReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
+               mbar_wait_warp(bar(kBarVReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
           if (!ok) break;
         }
-        if (!mbar_wait(bar(kBarVEmpty + s), par, &s_abort)) {
+        if (!mbar_wait_warp(bar(kBarVEmpty + s), par, &s_abort)) {
           ok = false;
           break;
         }
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tc = tcount + j;
             const int s = tc & 1;
             for (int kv = 0; kv < 2 && ok; ++kv) {
-              ok = mbar_wait(bar((kv ? kBarVFull : kBarKFull) + s), (tc >> 1) & 1, &s_abort);
+              ok = mbar_wait_warp(bar((kv ? kBarVFull : kBarKFull) + s), (tc >> 1) & 1, &s_abort);
               if (!ok) break;
               decode_fp8(g, tc, j, kv, part);
               fence_proxy_async();
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // quantised queries: all eight softmax warps turn both query tiles
       // into their e4m3 codes' values (element by element, in place) before
       // the MMA thread reads them
-      q_ok = mbar_wait(bar(kBarQFull), ucount & 1, &s_abort);
+      q_ok = mbar_wait_warp(bar(kBarQFull), ucount & 1, &s_abort);
       if (q_ok) {
         uint4* qt = reinterpret_cast<uint4*>(smem + kOffQ);
         for (int i = tid - 128; i < (int)(2 * kOperand / 16); i += 256) quantize_q8(qt + i, p.q_scale);
@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
         const uint32_t tc = tcount + j;
-        if (!mbar_wait(bar(kBarSFull + x), tc & 1, &s_abort)) {
+        if (!mbar_wait_warp(bar(kBarSFull + x), tc & 1, &s_abort)) {
           ok = false;
           break;
         }
@@ -633,19 +633,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = has_cap ? 1.f : xf.mul;  // raw score -> log2-domain logit
         uint32_t sr[128];
         tmem_ld128(tS, sr);
-        const bool full = valid == kN && key0 + kN - 1 <= pos && (W == 0 || pos - key0 < W);
         // logits in the log2 domain are fma(s, sc, -m): with a soft cap the
         // capped logit is formed first and sc is 1
-        if (has_cap) {
+        uint32_t dead = 0;  // (e4m3 caches) bit k: chunk k masked for every row of the warp
+        if constexpr (!FP8) {
+          const bool full = valid == kN && key0 + kN - 1 <= pos && (W == 0 || pos - key0 < W);
+          if (has_cap) {
 #pragma unroll
-          for (int c = 0; c < kN; ++c) sr[c] = __float_as_uint(xf(__uint_as_float(sr[c])));
-        }
-        if (!full) {
+            for (int c = 0; c < kN; ++c) sr[c] = __float_as_uint(xf(__uint_as_float(sr[c])));
+          }
+          if (!full) {
 #pragma unroll
-          for (int c = 0; c < kN; ++c) {
-            const int jk = key0 + c;
-            const bool okk = c < valid && jk <= pos && (W == 0 || pos - jk < W);
-            if (!okk) sr[c] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < kN; ++c) {
+              const int jk = key0 + c;
+              const bool okk = c < valid && jk <= pos && (W == 0 || pos - jk < W);
+              if (!okk) sr[c] = __float_as_uint(-INFINITY);
+            }
+          }
+        } else {
+          // e4m3 caches (compiled there only: in the bf16 kernels this path
+          // cost long-prefill throughput).  A tile that crosses a mask edge is
+          // taken in chunks of 16 keys: the rows of one warp are at most a few
+          // tokens apart, so a chunk is usually masked (or kept) whole for all
+          // of them -- a wholly masked chunk skips the cap and the mask (and,
+          // below, the exponentials), a wholly kept one the mask.  Whether the
+          // tile needs masking at all is decided for the whole warp (the rows'
+          // positions differ), so the warp collectives run in warp-uniform
+          // control flow.
+          const bool full = __all_sync(0xffffffffu, valid == kN && key0 + kN - 1 <= pos &&
+                                                        (W == 0 || pos - key0 < W));
+          if (full) {
+            if (has_cap) {
+#pragma unroll
+              for (int c = 0; c < kN; ++c) sr[c] = __float_as_uint(xf(__uint_as_float(sr[c])));
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kN / 16; ++k) {
+              const int c0 = 16 * k, j0 = key0 + c0, j1 = j0 + 15;
+              const bool row_dead = c0 >= valid || j0 > pos || (W > 0 && pos - j1 >= W);
+              const bool row_live = c0 + 15 < valid && j1 <= pos && (W == 0 || pos - j0 < W);
+              if (__all_sync(0xffffffffu, row_dead)) {
+                dead |= 1u << k;
+#pragma unroll
+                for (int c = c0; c < c0 + 16; ++c) sr[c] = __float_as_uint(-INFINITY);
+              } else {
+                if (has_cap) {
+#pragma unroll
+                  for (int c = c0; c < c0 + 16; ++c)
+                    sr[c] = __float_as_uint(xf(__uint_as_float(sr[c])));
+                }
+                if (!__all_sync(0xffffffffu, row_live)) {
+#pragma unroll
+                  for (int c = c0; c < c0 + 16; ++c) {
+                    const int jk = key0 + c;
+                    const bool okk = c < valid && jk <= pos && (W == 0 || pos - jk < W);
+                    if (!okk) sr[c] = __float_as_uint(-INFINITY);
+                  }
+                }
+              }
+            }
           }
         }
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -679,13 +726,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P packed as pairs into sr[0..kN/2): bf16, or fp16 with an e4m3 cache
         // (the values' type).  Scale-and-subtract uses packed f32x2
         // arithmetic, the exponentials the hardware ex2.
+        if (!FP8 || dead == 0) {
 #pragma unroll
-        for (int c = 0; c < kN; c += 2) {
-          const uint64_t x2 =
-              f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nm2);
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          sr[c >> 1] = pack_p<FP8>(fast_exp2(x0), fast_exp2(x1));
+          for (int c = 0; c < kN; c += 2) {
+            const uint64_t x2 =
+                f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nm2);
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            sr[c >> 1] = pack_p<FP8>(fast_exp2(x0), fast_exp2(x1));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kN / 16; ++k) {
+            if (dead & (1u << k)) {
+#pragma unroll
+              for (int c = 16 * k; c < 16 * k + 16; c += 2) sr[c >> 1] = 0u;  // P = 0
+            } else {
+#pragma unroll
+              for (int c = 16 * k; c < 16 * k + 16; c += 2) {
+                const uint64_t x2 =
+                    f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sc2, nm2);
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                sr[c >> 1] = pack_p<FP8>(fast_exp2(x0), fast_exp2(x1));
+              }
+            }
+          }
         }
         tmem_st64p(tS, sr);
         tc_fence_before();
@@ -716,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // epilogue: O / l -> bf16 rows
-      if (ok && !mbar_wait(bar(kBarODone + x), ucount & 1, &s_abort)) ok = false;
+      if (ok && !mbar_wait_warp(bar(kBarODone + x), ucount & 1, &s_abort)) ok = false;
       if (ok) {
         tc_fence_after();
         const float inv = (PH ? v_scale_of(p, g.h) : p.v_scale) / l_run;

@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto finalize_k = [&](uint32_t tc, int j) -> bool {
         const int s = tc & 1;
-        if (!mbar_wait(bar(kBarKFull + s), (tc >> 1) & 1, &s_abort)) return false;
+        if (!mbar_wait_warp(bar(kBarKFull + s), (tc >> 1) & 1, &s_abort)) return false;
         decode_fp8(g, tc, j, 0, 0);
         fence_proxy_async();
         __syncwarp();
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto finalize_v = [&](uint32_t tc, int j) -> bool {
         const int s = tc & 1;
-        if (!mbar_wait(bar(kBarVFull + s), (tc >> 1) & 1, &s_abort)) return false;
+        if (!mbar_wait_warp(bar(kBarVFull + s), (tc >> 1) & 1, &s_abort)) return false;
         if (FP8) {
           decode_fp8(g, tc, j, 1, 0);
           fence_proxy_async();
@@ -384,10 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j + 1 < nt) ids_next = load_ids(j + 1);
         if (FP8 && j >= 1) {
           ok = finalize_k(tc - 1, j - 1) &&
-               mbar_wait(bar(kBarKReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
+               mbar_wait_warp(bar(kBarKReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
           if (!ok) break;
         }
-        if (!mbar_wait(bar(kBarKEmpty + s), par, &s_abort)) {
+        if (!mbar_wait_warp(bar(kBarKEmpty + s), par, &s_abort)) {
           ok = false;
           break;
         }
@@ -395,10 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         (s ? k_last1 : k_last0) = (int)tc;
         if (FP8 && j >= 1) {
           ok = finalize_v(tc - 1, j - 1) &&
-               mbar_wait(bar(kBarVReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
+               mbar_wait_warp(bar(kBarVReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
           if (!ok) break;
         }
-        if (!mbar_wait(bar(kBarVEmpty + s), par, &s_abort)) {
+        if (!mbar_wait_warp(bar(kBarVEmpty + s), par, &s_abort)) {
           ok = false;
           break;
         }
@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t tc = tcount + j;
           const int s = tc & 1;
           for (int kv = 0; kv < 2 && ok; ++kv) {
-            ok = mbar_wait(bar((kv ? kBarVFull : kBarKFull) + s), (tc >> 1) & 1, &s_abort);
+            ok = mbar_wait_warp(bar((kv ? kBarVFull : kBarKFull) + s), (tc >> 1) & 1, &s_abort);
             if (!ok) break;
             decode_fp8(g, tc, j, kv, part);
             fence_proxy_async();
@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // quantised queries: the four softmax warps turn the query tile into
         // its e4m3 codes' values (element by element, in place) before the
         // MMA thread reads it
-        if (!mbar_wait(bar(kBarQFull), ucount & 1, &s_abort)) {
+        if (!mbar_wait_warp(bar(kBarQFull), ucount & 1, &s_abort)) {
           if (lane == 0) {
             set_status(hdr, RPA_STATUS_TIMEOUT);
             s_abort = 1;
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nt; ++j) {
         const uint32_t tc = tcount + j;
         const int s = tc & 1;
-        if (!mbar_wait(bar(kBarSFull + s), (tc >> 1) & 1, &s_abort)) {
+        if (!mbar_wait_warp(bar(kBarSFull + s), (tc >> 1) & 1, &s_abort)) {
           ok = false;
           break;
         }
@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // O holds P V of tiles < j once P V(j-1) is done: S(j) may have
           // completed before it, so wait for that product first
-          if (!mbar_wait(bar(kBarPVDone), (tc - 1) & 1, &s_abort)) {
+          if (!mbar_wait_warp(bar(kBarPVDone), (tc - 1) & 1, &s_abort)) {
             ok = false;
             break;
           }
@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // epilogue: O / l -> bf16 rows
-      if (ok && !mbar_wait(bar(kBarODone), ucount & 1, &s_abort)) ok = false;
+      if (ok && !mbar_wait_warp(bar(kBarODone), ucount & 1, &s_abort)) ok = false;
       if (ok) {
         tc_fence_after();
         const float inv = (PH ? v_scale_of(p, g.h) : p.v_scale) / l_run;
