@@ -372,6 +372,40 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
         const uint32_t cV = cK + kKeysPerWarp * Dp * 2;
         uint8_t* gK = smem + (cK - s_base);
         uint8_t* gV = smem + (cV - s_base);
+        // a stage whose 16 keys of this warp are all inside the unit and are
+        // not the new token (the usual case) converts in groups: the code
+        // loads of a group are issued before any conversion, so their
+        // latencies overlap
+        // (head_dim 64 only: at larger head_dims the group's registers spill)
+        const bool interior = D == 64 && kw >= du.k_begin && kw + kKeysPerWarp <= du.k_end &&
+                              !(ctx >= kw && ctx < kw + kKeysPerWarp);
+        if (D == 64 && interior) {
+          constexpr int kItems = 2 * kKeysPerWarp * (Dp / 8) / 32;  // chunks per lane
+          constexpr int kGroup = kItems < 8 ? kItems : 8;
+          const uint8_t* st8 = smem + (stage - s_base);
+#pragma unroll
+          for (int i0 = 0; i0 < kItems; i0 += kGroup) {
+            uint2 codes[kGroup];
+#pragma unroll
+            for (int i = 0; i < kGroup; ++i) {
+              const int idx = lane + 32 * (i0 + i);
+              const int kv = idx / (kKeysPerWarp * (Dp / 8));
+              const int rem = idx % (kKeysPerWarp * (Dp / 8));
+              const int r = rem / (Dp / 8), c = rem % (Dp / 8);
+              codes[i] = *reinterpret_cast<const uint2*>(
+                  st8 + (2 * (warp * kKeysPerWarp + r) + kv) * C::kRowBytes + c * 8);
+            }
+#pragma unroll
+            for (int i = 0; i < kGroup; ++i) {
+              const int idx = lane + 32 * (i0 + i);
+              const int kv = idx / (kKeysPerWarp * (Dp / 8));
+              const int rem = idx % (kKeysPerWarp * (Dp / 8));
+              const int r = rem / (Dp / 8), c = rem % (Dp / 8);
+              *reinterpret_cast<uint4*>((kv ? gV : gK) + swz(r, c, Dp * 2)) =
+                  kv ? dequant8_f16(codes[i]) : dequant8(codes[i]);
+            }
+          }
+        } else
         for (int idx = lane; idx < 2 * kKeysPerWarp * (Dp / 8); idx += 32) {
           const int kv = idx / (kKeysPerWarp * (Dp / 8));
           const int rem = idx % (kKeysPerWarp * (Dp / 8));
