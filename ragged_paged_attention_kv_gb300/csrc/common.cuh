@@ -24,19 +24,21 @@ enum HeaderWord {
   kHdrWords = 64,
 };
 
-// Decode unit: one (sequence, kv head, key split).
 // Decode unit: one (sequence, kv head, split of the key range).  The units of
 // one (seq, head) are contiguous, so split 0 of unit u is unit u - split.  The
-// sequence's token row q0 and kv_len ride along, so one load gives a unit.
-struct DecodeUnit {
+// sequence's token row q0 and kv_len ride along, so one load gives a unit
+// (16-byte aligned: two vector accesses move one).
+struct __align__(16) DecodeUnit {
   int32_t seq, head, k_begin, k_end;  // keys [k_begin, k_end) of this split
   int32_t split, nsplit, q0, kv_len;
 };
 
-// Prefill unit: one (sequence, tile of new tokens, kv head).
-struct PrefillUnit {
+// Prefill unit: one (sequence, tile of new tokens, kv head); one vector access.
+struct __align__(16) PrefillUnit {
   int32_t seq, t_begin, t_end, head;    // new tokens [t_begin, t_end) of seq
 };
+
+static_assert(sizeof(DecodeUnit) == 32 && sizeof(PrefillUnit) == 16, "unit sizes");
 
 // The planner splits a decode sequence's keys only when the batch has too
 // few (sequence, kv head) pairs to keep the GPU busy: splits aim at about

@@ -574,8 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sc = has_cap ? 1.f : xf.mul;  // raw score -> log2-domain logit
         const uint32_t tS = tmem + lane_off + kTmemS + 64 * s;
         uint32_t sr[kN];
-        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld64(tS, sr);
         const bool full = valid == kN && key0 + kN - 1 <= pos && (W == 0 || pos - key0 < W);
         if (has_cap) {
 #pragma unroll
