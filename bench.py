@@ -275,7 +275,7 @@ BOUNDS = {
 }
 
 
-def rooflines(w, work, dec_avg, pf_avg, peaks):
+def rooflines(w, work, dec_avg, pf_avg, peaks, name=None):
     """Per kernel: achieved vs peak.  The decode kernel is HBM-bound (its
     algorithmic bytes over its event time, against the measured copy
     bandwidth); the prefill kernel is a bf16 contraction (its flops over its
@@ -288,14 +288,16 @@ def rooflines(w, work, dec_avg, pf_avg, peaks):
                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": round(a / peaks["hbm_gbs"], 4),
                        "algorithmic_bytes": int(work["decode"]["bytes"]),
-                       "ms": round(dec_avg, 4)}
+                       "ms": round(dec_avg, 4),
+                       "traffic": traffic_for("decode.cu", name) if name else None}
     if work["prefill"]["tokens"]:
         a = work["prefill"]["flops"] / (pf_avg * 1e-3) / 1e12
         r["prefill"] = {"bound": "tensor", "kernel": prefill_kernel_name(w)[0],
                         "achieved": round(a, 1), "peak": peaks["bf16_tflops"],
                         "unit": "TFLOP/s", "frac": round(a / peaks["bf16_tflops"], 4),
                         "algorithmic_flops": int(work["prefill"]["flops"]),
-                        "ms": round(pf_avg, 4)}
+                        "ms": round(pf_avg, 4),
+                        "traffic": traffic_for(prefill_kernel_name(w)[1], name) if name else None}
     return r
 
 
@@ -445,7 +447,7 @@ def measure(name, args, world, rank, dev, flush, stream, with_e2e):
                        "decode": round(dec_avg, 4), "prefill": round(pf_avg, 4),
                        "step_with_kernel_events": round(statistics.mean(ms["step_serialised"]), 4)},
         "bound": BOUNDS.get(name, "hbm" if not work["prefill"]["tokens"] else "tensor"),
-        "rooflines": rooflines(w, work, dec_avg, pf_avg, peaks),
+        "rooflines": rooflines(w, work, dec_avg, pf_avg, peaks, name),
         "decode_kv_gbs": round(work["decode"]["bytes"] / (dec_avg * 1e-3) / 1e9, 1)
         if work["decode"]["tokens"] else None,
         "prefill_tflops": round(work["prefill"]["flops"] / (pf_avg * 1e-3) / 1e12, 2)
