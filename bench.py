@@ -272,6 +272,7 @@ BOUNDS = {
     "long_w4096": "tensor",
     "long_d256": "tensor",
     "fp8": "hbm, window-limited (67 MB of keys/values in the window): latency-dominated",
+    "fp8_w8a8": "as fp8; Q K^T of the prefill on e4m3 codes",
 }
 
 
@@ -468,7 +469,7 @@ def measure(name, args, world, rank, dev, flush, stream, with_e2e):
 
 # The configurations timed after the headline in the default run: the other
 # single-GPU configurations the metric is quoted on, plus head_dim 256.
-EXTRA_CONFIGS = ("mixed", "long", "long_w4096", "fp8", "decode_d256", "long_d256")
+EXTRA_CONFIGS = ("mixed", "long", "long_w4096", "fp8", "fp8_w8a8", "decode_d256", "long_d256")
 
 
 def gpu_arm(args, world, rank, local):

@@ -30,6 +30,13 @@
 // v3 _fetch_bkv does the same), in tiles aligned to ctx.  Value rows outside
 // a tile's valid range are zeroed before the PV product.  The unit's own new
 // tokens are written into their pages by the softmax warps.
+//
+// With an e4m3 cache, keys and values are decoded from their codes into the
+// MMA operands.  With quantised queries as well (q_scale, the w8a8 mode of
+// the ragged_paged_attention_v3 signature) S = Q K^T runs on the codes
+// themselves (tcgen05.mma kind::f8f6f4): the query tiles are quantised once
+// per unit, cached keys go from the page straight into the key stage, and
+// the logit scale carries q_scale * k_scale.
 #include "async.cuh"
 #include "common.cuh"
 #include "kv_write.cuh"
@@ -62,23 +69,50 @@ static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register sp
 // staging buffers that receive the pages' e4m3 codes ([128 rows][D] bytes)
 // before they are decoded into the bf16 operands: one per stage and operand
 // where they fit, else one per operand (head_dim 128).
-template <int D, bool FP8>
+// With quantised queries (Q8) the Q K^T product runs on the e4m3 codes
+// themselves: the query tiles become code tiles [128 rows][D bytes] (rows
+// swizzled over 128 bytes at head_dim 128, 64 at head_dim 64), the key stages
+// are code tiles too (cached pages land there as they are), and only the
+// values have staging buffers.  The bf16 query tiles are free once the codes
+// are formed; the step's new keys land there (stage s in tile s) as bf16
+// before they are quantised into their stage.
+template <int D, bool FP8, bool Q8 = false>
 struct TcCfg {
+  static_assert(!Q8 || FP8, "quantised queries need an e4m3 cache");
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kOperand = kHalves * kHalf;
   static constexpr uint32_t kStaging = FP8 ? 128u * D : 0u;
+  static constexpr uint32_t kTile8 = 128u * D;                    // one e4m3 code tile
+  static constexpr uint32_t kKStage = Q8 ? kTile8 : kOperand;     // key stage stride
+  static constexpr int kStgOps = Q8 ? 1 : 2;                      // operands with staging
+  static constexpr uint32_t kFixed = 4 * kOperand + 2 * kKStage + (Q8 ? 2 * kTile8 : 0);
   static constexpr uint32_t bytes_for(int stg) {
-    return (6 * kOperand + 2 * stg * kStaging + 1023) / 1024 * 1024 + 256 + 1024;
+    return (kFixed + kStgOps * stg * kStaging + 1023) / 1024 * 1024 + 256 + 1024;
   }
   static constexpr int kStgPerOp = !FP8 ? 0 : (bytes_for(2) <= 227 * 1024 ? 2 : 1);
   static constexpr uint32_t kOffQ = 0;                  // query tile X at kOffQ + X*kOperand
-  static constexpr uint32_t kOffK = 2 * kOperand;       // key stage s at kOffK + s*kOperand
-  static constexpr uint32_t kOffV = 4 * kOperand;       // value stage s at kOffV + s*kOperand
-  static constexpr uint32_t kOffStg = 6 * kOperand;     // staging (b, kv) at + (2b+kv)*kStaging
-  static constexpr uint32_t kOffBar = (kOffStg + 2 * kStgPerOp * kStaging + 1023) / 1024 * 1024;
+  static constexpr uint32_t kOffQ8 = 2 * kOperand;      // Q8: code tile X at kOffQ8 + X*kTile8
+  static constexpr uint32_t kOffK = 2 * kOperand + (Q8 ? 2 * kTile8 : 0);  // + s*kKStage
+  static constexpr uint32_t kOffV = kOffK + 2 * kKStage;                   // + s*kOperand
+  static constexpr uint32_t kOffStg = kOffV + 2 * kOperand;
+  static constexpr uint32_t kOffBar =
+      (kOffStg + kStgOps * kStgPerOp * kStaging + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = (int)kOffBar + 256 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "fits one CTA's shared memory");
+  static_assert(!Q8 || kStgPerOp == 2, "Q8: a value staging buffer per stage");
 };
+
+// Byte offset of the codes of elements 8*c8 .. 8*c8+7 of row r in an e4m3
+// code tile [128 rows][D bytes], in the swizzle the tensor map writes and
+// the MMA descriptor reads: 16-byte chunk (c8/2) of the row XOR-ed with
+// address bits 7-9 (128-byte swizzle, head_dim 128) or 7-8 (64-byte
+// swizzle, head_dim 64).
+template <int D>
+__device__ __forceinline__ uint32_t sw_e4m3(int r, int c8) {
+  static_assert(D == 64 || D == 128, "code tiles for head_dim 64 and 128");
+  const uint32_t phase = D == 128 ? (uint32_t)(r & 7) : (uint32_t)((r >> 1) & 3);
+  return (uint32_t)r * D + ((((uint32_t)c8 >> 1) ^ phase) << 4) + ((uint32_t)(c8 & 1) << 3);
+}
 
 enum Bar {
   kBarQFull = 0,    // both query tiles landed
@@ -101,6 +135,7 @@ struct TcMaps {
   CUtensorMap cache;  // pool [num_pages*P][2*Hkv][D], box {64, 1, min(P,128)} (fp8: {D, 1, ..})
   CUtensorMap knew;   // keys [T][Hkv][D], box {64, 1, 128}
   CUtensorMap vnew;   // values [T][Hkv][D], box {64, 1, 128}
+  CUtensorMap cache8; // Q8 only: the pool's codes, box {D, 1, min(P,128)}, swizzled as sw_e4m3
 };
 
 // Geometry of one unit, computed identically by every role.
@@ -149,10 +184,10 @@ __device__ __forceinline__ UnitGeom unit_geom(const AttnArgs& a, const PrefillUn
   return g;
 }
 
-template <int D, bool FP8, bool PH>
+template <int D, bool FP8, bool PH, bool Q8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ TcMaps maps, AttnArgs a) {
-  using C = TcCfg<D, FP8>;
+  using C = TcCfg<D, FP8, Q8>;
   // warps that decode fp8 operands: the TMA warp and warps 2, 3
   constexpr int kDecWarps = FP8 ? 3 : 1;
   constexpr uint32_t kOperand = C::kOperand, kOffQ = C::kOffQ, kOffK = C::kOffK,
@@ -215,13 +250,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&maps.cache);
     prefetch_tensormap(&maps.knew);
     prefetch_tensormap(&maps.vnew);
+    if (Q8) prefetch_tensormap(&maps.cache8);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  const uint32_t idesc_qk = idesc_bf16(kM, kN, false, false);
+  const uint32_t idesc_qk = Q8 ? idesc_e4m3(kM, kN) : idesc_bf16(kM, kN, false, false);
   // P and the values are fp16 with an e4m3 cache, bf16 otherwise
   const uint32_t idesc_pv = idesc_bf16(kM, D, false, true, FP8);
   const bool has_cap = p.logits_soft_cap > 0.f;
@@ -239,17 +275,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   // decoded in place so they carry exactly the codes the page write stores.
   // Value rows no row of the unit may see (past the valid range, or before
   // the window) become zero; key rows there are masked by the softmax.
+  // With Q8 only the values are staged and decoded; the keys stay e4m3
+  // codes (new keys are quantised from their bf16 landing buffer).
   auto staging = [&](uint32_t tc, int kv) -> uint32_t {
-    return C::kOffStg + (2 * (C::kStgPerOp == 2 ? (tc & 1) : 0) + kv) * C::kStaging;
+    return C::kOffStg +
+           (C::kStgOps * (C::kStgPerOp == 2 ? (tc & 1) : 0) + (Q8 ? 0 : kv)) * C::kStaging;
   };
   auto decode_fp8 = [&](const UnitGeom& g, uint32_t tc, int j, int kv, int part) {
     bool is_new;
     int key0, valid;
     g.tile(j, is_new, key0, valid);
-    uint8_t* op = smem + (kv ? kOffV : kOffK) + (tc & 1) * kOperand;
-    const uint8_t* stg = smem + staging(tc, kv);
     const float scale = !PH ? (kv ? p.v_scale : p.k_scale)
                             : (kv ? v_scale_of(p, g.h) : k_scale_of(p, g.h));
+    if constexpr (Q8) {
+      if (kv == 0) {
+        if (!is_new) return;  // cached codes landed in the key stage as they are
+        const uint8_t* src = smem + kOffQ + (tc & 1) * kOperand;
+        uint8_t* k8 = smem + kOffK + (tc & 1) * C::kKStage;
+        for (int idx = 32 * part + lane; idx < valid * (D / 8); idx += 32 * kDecWarps) {
+          const int r = idx / (D / 8), c = idx % (D / 8);
+          const uint4 v = *reinterpret_cast<const uint4*>(src + (c >> 3) * kHalf + sw128(r, c & 7));
+          *reinterpret_cast<uint2*>(k8 + sw_e4m3<D>(r, c)) = quantize8(v, scale);
+        }
+        return;
+      }
+    }
+    uint8_t* op = smem + (kv ? kOffV : kOffK) + (tc & 1) * (kv ? kOperand : C::kKStage);
+    const uint8_t* stg = smem + staging(tc, kv);
     const int rows = kv ? kN : valid;
     const int lead = kv ? g.lead(key0) : 0;
     for (int idx = 32 * part + lane; idx < rows * (D / 8); idx += 32 * kDecWarps) {
@@ -330,7 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool is_new;
         int key0, valid;
         g.tile(j, is_new, key0, valid);
-        const uint32_t dst = sb + (kv ? kOffV : kOffK) + s * kOperand;
+        // Q8: new keys land as bf16 in the (quantised, so free) query tile s
+        const uint32_t dst = sb + (kv                 ? kOffV + s * kOperand
+                                   : Q8 && is_new     ? kOffQ + s * kOperand
+                                                      : kOffK + s * C::kKStage);
         const uint32_t fullbar = bar((kv ? kBarVFull : kBarKFull) + s);
         if (is_new) {
           if (lane == 0) {
@@ -352,7 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int srow = P < kN ? (pg0 + lane) * P - key0 : 0;
             const int z = page * P + (P < kN ? 0 : key0 % P);
-            if (FP8) {
+            if (Q8 && kv == 0) {
+              tma_load_3d(dst + srow * D, &maps.cache8, fullbar, 0, 2 * g.h, z);
+            } else if (FP8) {
               tma_load_3d(sb + staging(tc, kv) + srow * D, &maps.cache, fullbar, 0, 2 * g.h + kv, z);
             } else {
               for (int hf = 0; hf < C::kHalves; ++hf)
@@ -408,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // codes of tile j-1 are decoded before those of tile j are fetched.
       constexpr bool kStg1 = FP8 && C::kStgPerOp == 1;
       bool ok = true;
+      bool landing_free = false;  // Q8: the query tiles are quantised, new keys may land
       int ids_next = load_ids(0);
       for (int j = 0; j < nt && ok; ++j) {
         const uint32_t tc = tcount + j;
@@ -425,6 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_warp(bar(kBarKEmpty + s), par, &s_abort)) {
           ok = false;
           break;
+        }
+        if (Q8 && !landing_free && j >= g.n_cached) {
+          if (!mbar_wait_warp(bar(kBarQReady), ucount & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          landing_free = true;
         }
         issue(j, 0, tc, ids);
         (s ? k_last1 : k_last0) = (int)tc;
@@ -475,8 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and its completion also tells the softmax of tile X that PV_X(j) is
       // done, so O_X may be rescaled.
       if (lane == 0) {
-        bool ok = mbar_wait(bar(FP8 && p.q_scale > 0.f ? kBarQReady : kBarQFull), ucount & 1,
-                            &s_abort);
+        bool ok = mbar_wait(bar(Q8 ? kBarQReady : kBarQFull), ucount & 1, &s_abort);
         tc_fence_after();
         auto qk = [&](uint32_t tc, int x, bool last_of_stage) -> bool {
           const int s = tc & 1;
@@ -485,12 +549,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               return false;
             tc_fence_after();
           }
-          const uint32_t sK = sb + kOffK + s * kOperand;
-          const uint32_t sQ = sb + kOffQ + x * kOperand;
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-            umma_ss(tmem + kTmemS + 128 * x, sdesc_sw128(sQ + off, 16, 1024),
-                    sdesc_sw128(sK + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+          const uint32_t sK = sb + kOffK + s * C::kKStage;
+          if constexpr (Q8) {
+            // e4m3 codes, 32 per product along the row (rows of D bytes)
+            const uint32_t sQ = sb + C::kOffQ8 + x * C::kTile8;
+            for (int k = 0; k < D / 32; ++k) {
+              const uint64_t ad = D == 128 ? sdesc_sw128(sQ + 32 * k, 16, 1024)
+                                           : sdesc_sw64(sQ + 32 * k, 16, 512);
+              const uint64_t bd = D == 128 ? sdesc_sw128(sK + 32 * k, 16, 1024)
+                                           : sdesc_sw64(sK + 32 * k, 16, 512);
+              umma_ss_e4m3(tmem + kTmemS + 128 * x, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+            }
+          } else {
+            const uint32_t sQ = sb + kOffQ + x * kOperand;
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+              umma_ss(tmem + kTmemS + 128 * x, sdesc_sw128(sQ + off, 16, 1024),
+                      sdesc_sw128(sK + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+            }
           }
           umma_commit(bar(kBarSFull + x));
           if (last_of_stage) umma_commit(bar(kBarKEmpty + s));
@@ -569,14 +645,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile B holds tokens t_begin + 128/G onwards; it may be empty
     const bool has_b = g.t_begin + kM / G < g.t_end;
     bool q_ok = true;
-    if (FP8 && p.q_scale > 0.f) {  // q_scale needs an e4m3 cache
-      // quantised queries: all eight softmax warps turn both query tiles
-      // into their e4m3 codes' values (element by element, in place) before
-      // the MMA thread reads them
+    if constexpr (Q8) {
+      // quantised queries: all eight softmax warps turn both bf16 query
+      // tiles into e4m3 code tiles (q / q_scale rounded to e4m3) before the
+      // MMA thread reads them and new keys land over the bf16 tiles
       q_ok = mbar_wait_warp(bar(kBarQFull), ucount & 1, &s_abort);
       if (q_ok) {
-        uint4* qt = reinterpret_cast<uint4*>(smem + kOffQ);
-        for (int i = tid - 128; i < (int)(2 * kOperand / 16); i += 256) quantize_q8(qt + i, p.q_scale);
+        constexpr int kChunks = D / 8;  // 8 elements per chunk
+        for (int i = tid - 128; i < 2 * kM * kChunks; i += 256) {
+          const int x = i / (kM * kChunks), r = (i / kChunks) % kM, c = i % kChunks;
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + kOffQ + x * kOperand +
+                                                          (c >> 3) * kHalf + sw128(r, c & 7));
+          *reinterpret_cast<uint2*>(smem + C::kOffQ8 + x * C::kTile8 + sw_e4m3<D>(r, c)) =
+              quantize8(v, p.q_scale);
+        }
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarQReady));
@@ -817,28 +899,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace tc
 
-template <int D, bool FP8, bool PH>
+template <int D, bool FP8, bool PH, bool Q8>
 static cudaError_t launch_prefill_tc_t(const AttnArgs& a, int max_units, int num_sms,
                                        cudaStream_t stream) {
-  using C = tc::TcCfg<D, FP8>;
+  using C = tc::TcCfg<D, FP8, Q8>;
   static std::atomic<unsigned long long> attr_done{0};
-  auto kern = tc::prefill_tc_kernel<D, FP8, PH>;
+  auto kern = tc::prefill_tc_kernel<D, FP8, PH, Q8>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, &attr_done);
   if (e != cudaSuccess) return e;
   const rpa_params_t& p = a.kv.p;
   const int G = p.num_q_heads / p.num_kv_heads;
-  tc::TcMaps maps;
+  tc::TcMaps maps{};
   const uint64_t T = (uint64_t)(p.total_tokens > 0 ? p.total_tokens : 1);
+  const uint64_t rows = (uint64_t)p.num_pages * p.page_size;
   const uint32_t prow = p.page_size < tc::kN ? (uint32_t)p.page_size : (uint32_t)tc::kN;
   bool ok = encode_map_3d(&maps.q, a.queries, 2, D, (uint64_t)p.num_q_heads, T, 64u, (uint32_t)G,
                           (uint32_t)(tc::kM / G), true) &&
             encode_map_3d(&maps.cache, a.kv.cache, FP8 ? 1 : 2, D, 2 * (uint64_t)p.num_kv_heads,
-                          (uint64_t)p.num_pages * p.page_size, FP8 ? (uint32_t)D : 64u, 1u, prow,
-                          !FP8) &&
+                          rows, FP8 ? (uint32_t)D : 64u, 1u, prow, !FP8) &&
             encode_map_3d(&maps.knew, a.kv.keys, 2, D, (uint64_t)p.num_kv_heads, T, 64u, 1u, 128u,
                           true) &&
             encode_map_3d(&maps.vnew, a.kv.values, 2, D, (uint64_t)p.num_kv_heads, T, 64u, 1u,
-                          128u, true);
+                          128u, true) &&
+            (!Q8 || encode_map_3d_swizzle(&maps.cache8, a.kv.cache, 1, D,
+                                          2 * (uint64_t)p.num_kv_heads, rows, (uint32_t)D, 1u,
+                                          prow, D));
   if (!ok) return cudaErrorInvalidValue;
   int grid = num_sms;
   if (grid > max_units) grid = max_units;
@@ -846,18 +931,26 @@ static cudaError_t launch_prefill_tc_t(const AttnArgs& a, int max_units, int num
   return launch_dependent(kern, grid, tc::kThreads, C::kSmemBytes, stream, maps, a);
 }
 
-cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream) {
-  const bool fp8 = a.kv.p.kv_dtype == RPA_KV_FP8_E4M3;
+template <int D>
+static cudaError_t launch_prefill_tc_d(const AttnArgs& a, int max_units, int num_sms,
+                                       cudaStream_t stream) {
+  const rpa_params_t& p = a.kv.p;
+  if (p.kv_dtype != RPA_KV_FP8_E4M3)
+    return launch_prefill_tc_t<D, false, false, false>(a, max_units, num_sms, stream);
   // per-head scales get their own instantiation, so the common cases keep
-  // their logit transform loop-invariant
-  const bool ph = a.kv.p.k_scale_heads != nullptr || a.kv.p.v_scale_heads != nullptr;
-  if (a.kv.p.head_dim == 64)
-    return !fp8 ? launch_prefill_tc_t<64, false, false>(a, max_units, num_sms, stream)
-           : ph  ? launch_prefill_tc_t<64, true, true>(a, max_units, num_sms, stream)
-                 : launch_prefill_tc_t<64, true, false>(a, max_units, num_sms, stream);
-  return !fp8 ? launch_prefill_tc_t<128, false, false>(a, max_units, num_sms, stream)
-         : ph  ? launch_prefill_tc_t<128, true, true>(a, max_units, num_sms, stream)
-               : launch_prefill_tc_t<128, true, false>(a, max_units, num_sms, stream);
+  // their logit transform loop-invariant; quantised queries (an e4m3 cache
+  // only) run Q K^T on the codes
+  const bool ph = p.k_scale_heads != nullptr || p.v_scale_heads != nullptr;
+  if (p.q_scale > 0.f)
+    return ph ? launch_prefill_tc_t<D, true, true, true>(a, max_units, num_sms, stream)
+              : launch_prefill_tc_t<D, true, false, true>(a, max_units, num_sms, stream);
+  return ph ? launch_prefill_tc_t<D, true, true, false>(a, max_units, num_sms, stream)
+            : launch_prefill_tc_t<D, true, false, false>(a, max_units, num_sms, stream);
+}
+
+cudaError_t launch_prefill_tc(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream) {
+  return a.kv.p.head_dim == 64 ? launch_prefill_tc_d<64>(a, max_units, num_sms, stream)
+                               : launch_prefill_tc_d<128>(a, max_units, num_sms, stream);
 }
 
 }  // namespace rpa

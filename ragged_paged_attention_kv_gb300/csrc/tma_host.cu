@@ -30,6 +30,13 @@ EncodeTiledFn encode_fn() {
 bool encode_map_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t dim0,
                    uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1, uint32_t box2,
                    bool swizzle128) {
+  return encode_map_3d_swizzle(map, base, elem_bytes, dim0, dim1, dim2, box0, box1, box2,
+                               swizzle128 ? 128 : 0);
+}
+
+bool encode_map_3d_swizzle(CUtensorMap* map, const void* base, int elem_bytes, uint64_t dim0,
+                           uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1,
+                           uint32_t box2, int swizzle_bytes) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {dim0, dim1, dim2};
@@ -40,7 +47,9 @@ bool encode_map_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t 
       elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                        : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -17,6 +17,10 @@ namespace rpa {
 bool encode_map_3d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t dim0,
                    uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1, uint32_t box2,
                    bool swizzle128);
+// The same with a chosen swizzle: 0 (none), 64 or 128 bytes.
+bool encode_map_3d_swizzle(CUtensorMap* map, const void* base, int elem_bytes, uint64_t dim0,
+                           uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1,
+                           uint32_t box2, int swizzle_bytes);
 
 // Sets the dynamic shared-memory limit of `func` once per device.
 cudaError_t ensure_smem_attr(const void* func, int bytes, std::atomic<unsigned long long>* done_mask);

@@ -274,6 +274,15 @@ POISON_CASES = [
                                                      head_dim=192, num_q_heads=16,
                                                      num_kv_heads=8, page_size=64,
                                                      sliding_window=300)),
+    # quantised queries: cached key codes go to the tensor core as they are
+    ("tc_q8_d128_window_partial_pages", lambda: _case("z17", 317, [1, 90, 33], [600, 500, 35],
+                                                      kv_dtype="fp8", k_scale=0.3, v_scale=0.1,
+                                                      q_scale=0.02, head_dim=128,
+                                                      page_size=64, sliding_window=300)),
+    ("tc_q8_d64_options", lambda: _case("z18", 318, [1, 1, 64, 20], [900, 129, 200, 21],
+                                        kv_dtype="fp8", k_scale=0.05, v_scale=0.07,
+                                        q_scale=0.02, num_q_heads=64, num_kv_heads=8,
+                                        logits_soft_cap=30.0, has_sink=True, page_size=8)),
 ]
 
 
@@ -367,6 +376,27 @@ Q8_CASES = [
                                      num_q_heads=8, num_kv_heads=2, logits_soft_cap=20.0)),
     ("mma_prefill_p4", lambda: _q8("q9", 509, [1, 25, 9], [90, 60, 40], page_size=4,
                                    sliding_window=20)),
+    # Q K^T on the e4m3 codes (tcgen05 prefill, head_dim 64 / 128): pages
+    # larger than a key tile, per-head scales, 8-token pages (the smallest
+    # page box of the code tiles), a window and a soft cap, and a long
+    # cached context with several new key tiles
+    ("tc_q8_d128_per_head_p256", lambda: _q8("q10", 510, [1, 260, 7], [1300, 900, 300],
+                                             head_dim=128, num_q_heads=32, num_kv_heads=4,
+                                             page_size=256,
+                                             k_scale_heads=[0.03, 0.06, 0.1, 0.2],
+                                             v_scale_heads=[0.05, 0.02, 0.08, 0.04])),
+    ("tc_q8_d64_p8_per_head_window", lambda: _q8("q11", 511, [3, 140, 1], [700, 400, 50],
+                                                 head_dim=64, num_q_heads=16, num_kv_heads=2,
+                                                 page_size=8, k_scale_heads=[0.03, 0.09],
+                                                 v_scale_heads=[0.05, 0.02], sliding_window=200,
+                                                 logits_soft_cap=25.0)),
+    ("tc_q8_d128_long_cached", lambda: _q8("q12", 512, [600, 1], [2000, 333], head_dim=128,
+                                           num_q_heads=8, num_kv_heads=2, page_size=32,
+                                           has_sink=True)),
+    ("tc_q8_d64_p128_many_units", lambda: _q8("q13", 513, [130, 70, 1, 257],
+                                              [1000, 70, 600, 900], head_dim=64,
+                                              num_q_heads=32, num_kv_heads=8, page_size=128,
+                                              sliding_window=500)),
 ]
 
 

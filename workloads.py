@@ -439,7 +439,9 @@ def long_small() -> Workload:
                     distribution=np.array([0, 0, 1], np.int32), total_tokens=L)
 
 
-def fp8() -> Workload:
+def fp8(q_scale: float = 0.0, name: str = "fp8") -> Workload:
+    """The fp8 e4m3 cache configuration; with q_scale > 0 the same batch in
+    the w8a8 mode (queries quantised to e4m3 with that scale)."""
     seed = 1005
     g = torch.Generator().manual_seed(seed)
     P = 16
@@ -451,13 +453,13 @@ def fp8() -> Workload:
     num_pages = int(math.ceil(need * 1.1))
     pps = -(-max(16384, 8192 + 256) // P)
     bt = _assign_pages(kv, P, num_pages, len(q), pps, g)
-    return Workload(name="fp8", seed=seed, num_q_heads=64, num_kv_heads=8, head_dim=64,
+    return Workload(name=name, seed=seed, num_q_heads=64, num_kv_heads=8, head_dim=64,
                     page_size=P, num_pages=num_pages, pages_per_seq=pps, max_num_seqs=len(q),
                     kv_dtype="fp8", softmax_scale=1.0 / 8.0, sliding_window=128,
                     logits_soft_cap=30.0, k_scale=0.05, v_scale=0.05, has_sink=True,
                     q_lens=q, kv_lens_valid=kv, block_tables=bt,
                     distribution=np.array([512, 520, 520], np.int32),
-                    total_tokens=int(q.sum()))
+                    total_tokens=int(q.sum()), q_scale=q_scale)
 
 
 def fp8_small() -> Workload:
@@ -491,6 +493,9 @@ WORKLOADS = {
     "long_w4096": lambda: long(4096),
     "long_small": long_small,
     "fp8": fp8,
+    # the fp8 batch with quantised queries: |q| of N(0,1) samples stays far
+    # below 448 * 0.02, so no query code saturates
+    "fp8_w8a8": lambda: fp8(0.02, "fp8_w8a8"),
     "fp8_small": fp8_small,
     "decode_d256": decode_d256,
     "decode_d256_small": lambda: decode_d256(64, "decode_d256_small"),
