@@ -266,8 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Every role runs this loop over the CTA's units with its own body, so
   // the code of each role stays within its register budget; all threads meet
-  // at the same two barriers per unit.  tcount counts the key tiles and
-  // ucount the units the CTA has processed so far (all roles agree).
+  // at the same two barriers per unit.  The counters (all roles agree) give
+  // the mbarrier phases: tcount counts the key tiles and ucount the units
+  // the CTA has processed so far, for the barriers every unit uses; tcount_b
+  // and ucount_b count only the units with a query tile B, for tile B's
+  // own barriers (S full, P ready, O done), which other units leave alone.
   // fp8 cache: the staging buffer of an operand of tile tc, and the decoding
   // of a landed operand of tile j into its bf16 stage, shared by kDecWarps
   // warps (part 0..kDecWarps-1).  Cached rows are decoded from their e4m3
@@ -321,17 +324,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
+  struct Counts {
+    uint32_t tcount, ucount, tcount_b, ucount_b;
+    // phase counters of query tile x's own barriers
+    __device__ uint32_t tiles(int x) const { return x ? tcount_b : tcount; }
+    __device__ uint32_t units(int x) const { return x ? ucount_b : ucount; }
+  };
   auto unit_loop = [&](auto&& body) {
-    uint32_t tcount = 0, ucount = 0;
+    Counts n{0, 0, 0, 0};
     for (;;) {
       if (tid == 0) s_unit = atomicAdd(hdr + kHdrPrefillNext, 1);
       __syncthreads();
       const int u = s_unit;
       if (u >= n_units || s_abort) break;
       const UnitGeom g = unit_geom(a, units[u]);
-      body(g, tcount, ucount);
-      tcount += g.n_tiles;
-      ucount += 1;
+      body(g, n);
+      n.tcount += g.n_tiles;
+      n.ucount += 1;
+      if (g.t_begin + kM / G < g.t_end) {  // the unit has a query tile B
+        n.tcount_b += g.n_tiles;
+        n.ucount_b += 1;
+      }
       tc_fence_before();
       __syncthreads();  // the next unit reuses Q, the stages and tensor memory
       tc_fence_after();
@@ -344,7 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the last query copy (unit count) and the last key / value copy (tile
       // count) per stage this warp issued, for the drain at exit
       int q_last = -1, k_last0 = -1, k_last1 = -1, v_last0 = -1, v_last1 = -1;
-      unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t ucount) {
+      unit_loop([&](const UnitGeom& g, const Counts& n) {
+      const uint32_t tcount = n.tcount, ucount = n.ucount;
       const int nt = g.n_tiles;
       // ------------------------------------------------------- TMA producer
       // Keys of tile j go into key stage j%2 once both S products of tile
@@ -530,7 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!drained) set_status(hdr, RPA_STATUS_TIMEOUT);
       }
     } else if (warp == 1) {
-      unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t ucount) {
+      unit_loop([&](const UnitGeom& g, const Counts& n) {
+      const uint32_t tcount = n.tcount, ucount = n.ucount;
       const int nt = g.n_tiles;
       const bool has_b = g.t_begin + kM / G < g.t_end;
       // ------------------------------------------------------------ MMA
@@ -574,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto pv = [&](uint32_t tc, int j, int x, bool last_of_stage) -> bool {
           const int s = tc & 1;
-          if (!mbar_wait(bar(kBarPReady + x), tc & 1, &s_abort)) return false;
+          if (!mbar_wait(bar(kBarPReady + x), (n.tiles(x) + j) & 1, &s_abort)) return false;
           if (x == 0 && !mbar_wait(bar(kBarVReady + s), (tc >> 1) & 1, &s_abort)) return false;
           tc_fence_after();
           const uint32_t sV = sb + kOffV + s * kOperand;
@@ -615,7 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (FP8) {
         // warps 2 and 3: their shares of the fp8 decoding, tile by tile
         const int part = warp - 1;
-        unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t) {
+        unit_loop([&](const UnitGeom& g, const Counts& n) {
+          const uint32_t tcount = n.tcount;
           bool ok = true;
           for (int j = 0; j < g.n_tiles && ok; ++j) {
             const uint32_t tc = tcount + j;
@@ -635,12 +651,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         });
       } else {
-        unit_loop([](const UnitGeom&, uint32_t, uint32_t) {});
+        unit_loop([](const UnitGeom&, const Counts&) {});
       }
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    unit_loop([&](const UnitGeom& g, const uint32_t tcount, const uint32_t ucount) {
+    unit_loop([&](const UnitGeom& g, const Counts& n) {
+    const uint32_t ucount = n.ucount;
     const int nt = g.n_tiles;
     // tile B holds tokens t_begin + 128/G onwards; it may be empty
     const bool has_b = g.t_begin + kM / G < g.t_end;
@@ -695,8 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l_run = a.sink ? 1.f : 0.f;
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
-        const uint32_t tc = tcount + j;
-        if (!mbar_wait_warp(bar(kBarSFull + x), tc & 1, &s_abort)) {
+        if (!mbar_wait_warp(bar(kBarSFull + x), (n.tiles(x) + j) & 1, &s_abort)) {
           ok = false;
           break;
         }
@@ -864,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // epilogue: O / l -> bf16 rows
-      if (ok && !mbar_wait_warp(bar(kBarODone + x), ucount & 1, &s_abort)) ok = false;
+      if (ok && !mbar_wait_warp(bar(kBarODone + x), n.units(x) & 1, &s_abort)) ok = false;
       if (ok) {
         tc_fence_after();
         const float inv = (PH ? v_scale_of(p, g.h) : p.v_scale) / l_run;

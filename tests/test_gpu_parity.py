@@ -405,6 +405,32 @@ def test_quantised_query_cases(name, make):
     check_case(make())
 
 
+# More units than CTAs, with ragged tails: the planner emits each (sequence,
+# head)'s tail unit (often a single query tile) ahead of its full units, so
+# CTAs take tail units and full units one after another, and the tails'
+# tile counts are odd and even.
+MANY_UNIT_CASES = [
+    ("bf16_d128", lambda: _case("mu1", 901, [130] * 12 + [2] * 30,
+                                [230, 430, 830, 260, 388, 1000, 131, 700, 515, 977, 300, 250]
+                                + [100 + 37 * i for i in range(30)],
+                                num_q_heads=32, num_kv_heads=8, head_dim=128)),
+    ("fp8_d64", lambda: _case("mu2", 902, [40] * 20 + [3] * 24,
+                              [100 + 61 * i for i in range(20)] + [50 + 90 * i for i in range(24)],
+                              num_q_heads=64, num_kv_heads=8, head_dim=64, kv_dtype="fp8",
+                              k_scale=0.05, v_scale=0.07, has_sink=True)),
+    ("fp8_q8_d128", lambda: _case("mu3", 903, [130] * 12 + [2] * 30,
+                                  [230, 430, 830, 260, 388, 1000, 131, 700, 515, 977, 300, 250]
+                                  + [100 + 37 * i for i in range(30)],
+                                  num_q_heads=32, num_kv_heads=8, head_dim=128, kv_dtype="fp8",
+                                  k_scale=0.05, v_scale=0.07, q_scale=0.02)),
+]
+
+
+@pytest.mark.parametrize("name,make", MANY_UNIT_CASES, ids=[c[0] for c in MANY_UNIT_CASES])
+def test_many_units_with_ragged_tails(name, make):
+    check_case(make())
+
+
 def test_decode_split_boundaries():
     # kv lengths at page and split boundaries, all decode, big enough batch that
     # the planner's split size stays at its minimum
