@@ -57,6 +57,8 @@ DESCRIPTIONS = {
                   "Hq32/Hkv8/D128, bf16, page_size 64",
     "fp8": "fp8 e4m3 cache (k/v scale 0.05), soft cap 30, sinks, window 128: 512 decode "
            "(kv~U[256,16384]) + 8x256 chunks (prior kv~U[0,8192]); Hq64/Hkv8/D64, page_size 16",
+    "fp8_w8a8": "the fp8 batch with quantised queries (q_scale 0.02, w8a8): Q K^T of the "
+                "prefill on the e4m3 codes",
     "decode_small": "decode shape at 64 seqs (profiling size): q_len=1, kv_len~U[512,4096]; "
                     "Hq32/Hkv8/D128, bf16, page_size 16, pool = pages used + 10%",
     "long_small": "long-context shape at profiling size: 1 seq q=kv=8192 causal; Hq32/Hkv8/D128, "
