@@ -17,8 +17,8 @@ is the max over ranks, and value counts the tokens of all ranks.
 
 The default run times the decode workload (the headline: value, e2e,
 roofline) and then, under "configs", the mixed, long, long_w4096, fp8,
-decode_d256 and long_d256 workloads, each with its own step time, kernel
-times, clocks and per-kernel rooflines.
+fp8_w8a8, decode_d256 and long_d256 workloads, each with its own step time,
+kernel times, clocks and per-kernel rooflines.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle instead
 (on the host cores, a bounded sample of the same workload per step).
