@@ -63,6 +63,8 @@ DESCRIPTIONS = {
                     "Hq32/Hkv8/D128, bf16, page_size 16, pool = pages used + 10%",
     "long_small": "long-context shape at profiling size: 1 seq q=kv=8192 causal; Hq32/Hkv8/D128, "
                   "bf16, page_size 64",
+    "long_small_fp8": "long_small with an e4m3 cache (k/v scale 0.05): 1 seq q=kv=8192 causal; "
+                      "Hq32/Hkv8/D128, page_size 64 (profiling size)",
     "fp8_small": "fp8 shape at profiling size: 64 decode + 8x256 chunks; e4m3 cache, cap 30, "
                  "sinks, window 128; Hq64/Hkv8/D64, page_size 16",
     "tiny": "tiny mixed batch: 3 seqs (1,17),(24,24),(5,40); Hq4/Hkv2/D64/P16",

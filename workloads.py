@@ -422,8 +422,9 @@ def long_d256() -> Workload:
                     distribution=np.array([0, 0, 2], np.int32), total_tokens=2 * L)
 
 
-def long_small() -> Workload:
-    """The long-context shape at one sequence of 8192 tokens (profiling size)."""
+def long_small(kv_dtype: str = "bf16", name: str = "long_small") -> Workload:
+    """The long-context shape at one sequence of 8192 tokens (profiling size);
+    with kv_dtype "fp8" the same prefill into an e4m3 cache (k/v scale 0.05)."""
     seed = 1014
     g = torch.Generator().manual_seed(seed)
     P, L = 64, 8192
@@ -431,10 +432,12 @@ def long_small() -> Workload:
     kv = np.full(1, L, np.int32)
     pps = L // P
     bt = _assign_pages(kv, P, 256, 1, pps, g)
-    return Workload(name="long_small", seed=seed, num_q_heads=32, num_kv_heads=8, head_dim=128,
+    fp8 = kv_dtype == "fp8"
+    return Workload(name=name, seed=seed, num_q_heads=32, num_kv_heads=8, head_dim=128,
                     page_size=P, num_pages=256, pages_per_seq=pps, max_num_seqs=1,
-                    kv_dtype="bf16", softmax_scale=1.0 / math.sqrt(128), sliding_window=0,
-                    logits_soft_cap=0.0, k_scale=1.0, v_scale=1.0, has_sink=False,
+                    kv_dtype=kv_dtype, softmax_scale=1.0 / math.sqrt(128), sliding_window=0,
+                    logits_soft_cap=0.0, k_scale=0.05 if fp8 else 1.0,
+                    v_scale=0.05 if fp8 else 1.0, has_sink=False,
                     q_lens=q, kv_lens_valid=kv, block_tables=bt,
                     distribution=np.array([0, 0, 1], np.int32), total_tokens=L)
 
@@ -492,6 +495,7 @@ WORKLOADS = {
     "long": lambda: long(0),
     "long_w4096": lambda: long(4096),
     "long_small": long_small,
+    "long_small_fp8": lambda: long_small("fp8", "long_small_fp8"),
     "fp8": fp8,
     # the fp8 batch with quantised queries: |q| of N(0,1) samples stays far
     # below 448 * 0.02, so no query code saturates
