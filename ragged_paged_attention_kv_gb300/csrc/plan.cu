@@ -12,6 +12,8 @@
 
 #include "common.cuh"
 #include "kv_write.cuh"
+#include "launch.h"
+#include "tma_host.h"
 
 namespace rpa {
 
@@ -323,6 +325,98 @@ cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int
   else
     plan_kernel<1024><<<1, 1024, 0, stream>>>(p, kv_lens, qsl, dist, ws, prefill_rows);
   return cudaGetLastError();
+}
+
+// Page write ahead of the attention kernels (e4m3 cache, head_dim 64/128
+// tcgen05 prefill).  The new tokens of every sequence the planner gives to
+// the prefill kernel -- the planner's own classification, on the same
+// metadata -- are quantised into their pages once, so that kernel reads every
+// key and value tile from the pool as codes and no unit quantises a tile of
+// new tokens again.  It runs right behind the planner and overlaps it: it
+// needs only the metadata, which it checks itself (invalid sequences and
+// out-of-range page ids are skipped; the prefill kernel reads, checks and
+// reports the same block-table entries when it loads those tiles).  It
+// completes only after the planner, so the kernel waiting for it also finds
+// the plan.  Each warp takes a contiguous run of tokens: it finds the
+// sequence of its first token with a 32-way search of query_start_loc, then
+// walks forward, and writes every kv head's key and value row of each token
+// (one 16-byte chunk of bf16 inputs per lane and step, four steps in flight).
+template <int D>
+__global__ void __launch_bounds__(256) prefill_pages_kernel(KvArgs a, const int32_t* kv_lens,
+                                                            const int32_t* qsl,
+                                                            const int32_t* dist) {
+  griddep_launch_dependents();  // the decode kernel waits for this grid itself
+  const rpa_params_t& p = a.p;
+  const int lane = threadIdx.x & 31;
+  const int d0 = __ldg(dist), d1 = __ldg(dist + 1), d2 = __ldg(dist + 2);
+  const int S = (0 <= d0 && d0 <= d1 && d1 <= d2 && d2 <= p.max_num_seqs) ? d2 : 0;
+  const int T = p.total_tokens;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int per = (T + warps - 1) / warps;
+  const int t0 = gw * per, t1 = min(T, t0 + per);
+  if (S > 0 && t0 < t1) {
+    // the last sequence s < S with query_start_loc[s] <= t0
+    int lo = 0, hi = S;
+    while (hi - lo > 1) {
+      const int step = (hi - lo + 31) / 32;
+      const int idx = lo + lane * step;
+      const unsigned m = __ballot_sync(0xffffffffu, idx < hi && __ldg(qsl + idx) <= t0);
+      lo += m ? (31 - __clz(m)) * step : 0;
+      hi = min(hi, lo + step);
+    }
+    int s = lo;
+    SeqPlan sp = classify(p, s, d0, load_meta(s, kv_lens, qsl));
+    int a_s = __ldg(qsl + s), b_s = __ldg(qsl + s + 1);
+    constexpr int kChunks = D / 8, kU = 4;
+    const int Hkv = p.num_kv_heads;
+    const int items = Hkv * 2 * kChunks;  // (head, key / value, chunk) of one token
+    for (int t = t0; t < t1; ++t) {
+      while (t >= b_s && s + 1 < S) {
+        ++s;
+        sp = classify(p, s, d0, load_meta(s, kv_lens, qsl));
+        a_s = __ldg(qsl + s);
+        b_s = __ldg(qsl + s + 1);
+      }
+      if (sp.cls != 2 || t < a_s || t >= b_s) continue;
+      const int pos = sp.kv_len - sp.q_len + (t - sp.q0);
+      const int page = __ldg(a.block_tables + (int64_t)s * p.pages_per_seq + pos / p.page_size);
+      if (page < 0 || page >= p.num_pages) continue;
+      const int row = pos % p.page_size;
+      for (int i0 = 0; i0 < items; i0 += 32 * kU) {
+        uint4 x[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int i = i0 + 32 * u + lane;
+          if (i < items) {
+            const int h = i / (2 * kChunks), kv = (i / kChunks) & 1, c = i % kChunks;
+            x[u] = __ldg(reinterpret_cast<const uint4*>(
+                (kv ? a.values : a.keys) + ((int64_t)t * Hkv + h) * D + c * 8));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int i = i0 + 32 * u + lane;
+          if (i < items) {
+            const int h = i / (2 * kChunks), kv = (i / kChunks) & 1, c = i % kChunks;
+            *reinterpret_cast<uint2*>(a.cache + pool_offset(p, page, row, 2 * h + kv, 1) + c * 8) =
+                quantize8(x[u], kv ? v_scale_of(p, h) : k_scale_of(p, h));
+          }
+        }
+      }
+    }
+  }
+  griddep_wait();  // complete only after the planner
+}
+
+cudaError_t launch_prefill_pages(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,
+                                 const int32_t* dist, int num_sms, cudaStream_t stream) {
+  const int T = a.p.total_tokens > 0 ? a.p.total_tokens : 1;
+  int grid = (T + 7) / 8;  // at least one token per warp
+  if (grid > 2 * num_sms) grid = 2 * num_sms;
+  if (a.p.head_dim == 64)
+    return launch_dependent(prefill_pages_kernel<64>, grid, 256, 0, stream, a, kv_lens, qsl, dist);
+  return launch_dependent(prefill_pages_kernel<128>, grid, 256, 0, stream, a, kv_lens, qsl, dist);
 }
 
 cudaError_t launch_cache_write(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,

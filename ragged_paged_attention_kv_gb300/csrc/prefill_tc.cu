@@ -31,7 +31,10 @@
 // a tile's valid range are zeroed before the PV product.  The unit's own new
 // tokens are written into their pages by the softmax warps.
 //
-// With an e4m3 cache, keys and values are decoded from their codes into the
+// With an e4m3 cache the step's new tokens are quantised into their pages
+// once, by a small kernel ahead of this one, and every key and value tile
+// comes from the pool as codes (a tile of new tokens is read by many units:
+// each would otherwise quantise it again); the codes are decoded into the
 // MMA operands.  With quantised queries as well (q_scale, the w8a8 mode of
 // the ragged_paged_attention_v3 signature) S = Q K^T runs on the codes
 // themselves (tcgen05.mma kind::f8f6f4): the query tiles are quantised once
@@ -72,10 +75,8 @@ static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register sp
 // With quantised queries (Q8) the Q K^T product runs on the e4m3 codes
 // themselves: the query tiles become code tiles [128 rows][D bytes] (rows
 // swizzled over 128 bytes at head_dim 128, 64 at head_dim 64), the key stages
-// are code tiles too (cached pages land there as they are), and only the
-// values have staging buffers.  The bf16 query tiles are free once the codes
-// are formed; the step's new keys land there (stage s in tile s) as bf16
-// before they are quantised into their stage.
+// are code tiles too (the pages' codes land there as they are), and only the
+// values have staging buffers.
 template <int D, bool FP8, bool Q8 = false>
 struct TcCfg {
   static_assert(!Q8 || FP8, "quantised queries need an e4m3 cache");
@@ -138,18 +139,22 @@ struct TcMaps {
   CUtensorMap cache8; // Q8 only: the pool's codes, box {D, 1, min(P,128)}, swizzled as sw_e4m3
 };
 
-// Geometry of one unit, computed identically by every role.
+// Geometry of one unit, computed identically by every role.  Keys
+// [c_start, k_end) come from the pool in 128-key tiles aligned to 128 (k_end
+// = ctx, or with an e4m3 cache the unit's last position + 1: the step's new
+// tokens are already in their pages), the rest from the keys/values inputs in
+// tiles aligned to ctx.
 struct UnitGeom {
   int seq, h, q0, q_len, kv_len, ctx, t_begin, t_end;
   int lo;              // first key any row of the tile may see
-  int c_start, n_cached, i0, n_tiles;
+  int c_start, k_end, n_cached, i0, n_tiles;
   // rows of a tile starting at key0 that lie before every row's window
   __device__ int lead(int key0) const { return lo > key0 ? lo - key0 : 0; }
   __device__ void tile(int j, bool& is_new, int& key0, int& valid) const {
     if (j < n_cached) {
       is_new = false;
       key0 = c_start + kN * j;
-      valid = min(kN, ctx - key0);
+      valid = min(kN, k_end - key0);
     } else {
       is_new = true;
       key0 = ctx + kN * (i0 + j - n_cached);
@@ -158,6 +163,7 @@ struct UnitGeom {
   }
 };
 
+template <bool FROM_PAGES>
 __device__ __forceinline__ UnitGeom unit_geom(const AttnArgs& a, const PrefillUnit& pu) {
   UnitGeom g;
   g.seq = pu.seq;
@@ -171,16 +177,17 @@ __device__ __forceinline__ UnitGeom unit_geom(const AttnArgs& a, const PrefillUn
   const int W = a.kv.p.sliding_window;
   const int pos_first = g.ctx + g.t_begin, pos_last = g.ctx + g.t_end - 1;
   g.lo = (W > 0 && pos_first - W + 1 > 0) ? pos_first - W + 1 : 0;
-  if (g.lo < g.ctx) {
+  g.k_end = FROM_PAGES ? pos_last + 1 : g.ctx;
+  if (g.lo < g.k_end) {
     g.c_start = g.lo & ~(kN - 1);
-    g.n_cached = (g.ctx - g.c_start + kN - 1) / kN;
+    g.n_cached = (g.k_end - g.c_start + kN - 1) / kN;
   } else {
     g.c_start = 0;
     g.n_cached = 0;
   }
   g.i0 = g.lo > g.ctx ? (g.lo - g.ctx) / kN : 0;
   const int i1 = (pos_last - g.ctx) / kN;
-  g.n_tiles = g.n_cached + (i1 - g.i0 + 1);
+  g.n_tiles = g.n_cached + (FROM_PAGES ? 0 : i1 - g.i0 + 1);
   return g;
 }
 
@@ -272,37 +279,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // and ucount_b count only the units with a query tile B, for tile B's
   // own barriers (S full, P ready, O done), which other units leave alone.
   // fp8 cache: the staging buffer of an operand of tile tc, and the decoding
-  // of a landed operand of tile j into its bf16 stage, shared by kDecWarps
-  // warps (part 0..kDecWarps-1).  Cached rows are decoded from their e4m3
-  // codes; new rows, which came as bf16 from the inputs, are quantised and
-  // decoded in place so they carry exactly the codes the page write stores.
-  // Value rows no row of the unit may see (past the valid range, or before
-  // the window) become zero; key rows there are masked by the softmax.
-  // With Q8 only the values are staged and decoded; the keys stay e4m3
-  // codes (new keys are quantised from their bf16 landing buffer).
+  // of a landed operand of tile j into its stage, shared by kDecWarps warps
+  // (part 0..kDecWarps-1).  Every tile of an e4m3 unit comes from the pages
+  // (the step's new tokens were written there ahead of this kernel): keys
+  // are decoded to bf16 (the queries' type), values to fp16 (exact for e4m3,
+  // so that the P V product carries P in fp16).  Value rows no row of the
+  // unit may see (past the valid range, or before the window) become zero;
+  // key rows there are masked by the softmax.  With Q8 only the values are
+  // staged and decoded; the keys land as codes in their stage.
   auto staging = [&](uint32_t tc, int kv) -> uint32_t {
     return C::kOffStg +
            (C::kStgOps * (C::kStgPerOp == 2 ? (tc & 1) : 0) + (Q8 ? 0 : kv)) * C::kStaging;
   };
   auto decode_fp8 = [&](const UnitGeom& g, uint32_t tc, int j, int kv, int part) {
+    if (Q8 && kv == 0) return;
     bool is_new;
     int key0, valid;
     g.tile(j, is_new, key0, valid);
-    const float scale = !PH ? (kv ? p.v_scale : p.k_scale)
-                            : (kv ? v_scale_of(p, g.h) : k_scale_of(p, g.h));
-    if constexpr (Q8) {
-      if (kv == 0) {
-        if (!is_new) return;  // cached codes landed in the key stage as they are
-        const uint8_t* src = smem + kOffQ + (tc & 1) * kOperand;
-        uint8_t* k8 = smem + kOffK + (tc & 1) * C::kKStage;
-        for (int idx = 32 * part + lane; idx < valid * (D / 8); idx += 32 * kDecWarps) {
-          const int r = idx / (D / 8), c = idx % (D / 8);
-          const uint4 v = *reinterpret_cast<const uint4*>(src + (c >> 3) * kHalf + sw128(r, c & 7));
-          *reinterpret_cast<uint2*>(k8 + sw_e4m3<D>(r, c)) = quantize8(v, scale);
-        }
-        return;
-      }
-    }
     uint8_t* op = smem + (kv ? kOffV : kOffK) + (tc & 1) * (kv ? kOperand : C::kKStage);
     const uint8_t* stg = smem + staging(tc, kv);
     const int rows = kv ? kN : valid;
@@ -310,13 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = 32 * part + lane; idx < rows * (D / 8); idx += 32 * kDecWarps) {
       const int r = idx / (D / 8), c = idx % (D / 8);
       uint4* dst = reinterpret_cast<uint4*>(op + (c >> 3) * kHalf + sw128(r, c & 7));
-      // keys become bf16 (the queries' type); values fp16, exact for e4m3,
-      // so that the P V product carries P in fp16
       if (r >= valid || r < lead) {
         *dst = make_uint4(0, 0, 0, 0);
-      } else if (is_new) {
-        const uint2 codes = quantize8(*dst, scale);
-        *dst = kv ? dequant8_f16(codes) : dequant8(codes);
       } else {
         const uint2 codes = *reinterpret_cast<const uint2*>(stg + r * D + c * 8);
         *dst = kv ? dequant8_f16(codes) : dequant8(codes);
@@ -337,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       const int u = s_unit;
       if (u >= n_units || s_abort) break;
-      const UnitGeom g = unit_geom(a, units[u]);
+      const UnitGeom g = unit_geom<FP8>(a, units[u]);
       body(g, n);
       n.tcount += g.n_tiles;
       n.ucount += 1;
@@ -396,10 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool is_new;
         int key0, valid;
         g.tile(j, is_new, key0, valid);
-        // Q8: new keys land as bf16 in the (quantised, so free) query tile s
-        const uint32_t dst = sb + (kv                 ? kOffV + s * kOperand
-                                   : Q8 && is_new     ? kOffQ + s * kOperand
-                                                      : kOffK + s * C::kKStage);
+        const uint32_t dst = sb + (kv ? kOffV + s * kOperand : kOffK + s * C::kKStage);
         const uint32_t fullbar = bar((kv ? kBarVFull : kBarKFull) + s);
         if (is_new) {
           if (lane == 0) {
@@ -479,7 +464,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // codes of tile j-1 are decoded before those of tile j are fetched.
       constexpr bool kStg1 = FP8 && C::kStgPerOp == 1;
       bool ok = true;
-      bool landing_free = false;  // Q8: the query tiles are quantised, new keys may land
       int ids_next = load_ids(0);
       for (int j = 0; j < nt && ok; ++j) {
         const uint32_t tc = tcount + j;
@@ -497,13 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_warp(bar(kBarKEmpty + s), par, &s_abort)) {
           ok = false;
           break;
-        }
-        if (Q8 && !landing_free && j >= g.n_cached) {
-          if (!mbar_wait_warp(bar(kBarQReady), ucount & 1, &s_abort)) {
-            ok = false;
-            break;
-          }
-          landing_free = true;
         }
         issue(j, 0, tc, ids);
         (s ? k_last1 : k_last0) = (int)tc;
@@ -700,8 +677,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // this unit's new tokens -> their pages (an eighth of them per warp, a
       // quarter when tile B is empty); the loads are batched, so the write
-      // fits in the time the first S tile of the unit takes to arrive
-      {
+      // fits in the time the first S tile of the unit takes to arrive.  An
+      // e4m3 cache had its new tokens written ahead of this kernel.
+      if constexpr (!FP8) {
         const int n = g.t_end - g.t_begin, nw = has_b ? 8 : 4, w = warp - 4;
         const int i0 = n * w / nw, i1 = n * (w + 1) / nw;
         write_tokens_kv<FP8, D, 4>(a.kv, g.seq, g.q0 + g.t_begin + i0, g.ctx + g.t_begin + i0,
