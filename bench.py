@@ -271,7 +271,9 @@ def prefill_kernel_name(w):
 BOUNDS = {
     "decode": "hbm",
     "decode_d256": "hbm",
-    "mixed": "hbm (decode share) + tensor (prefill share)",
+    "mixed": "hbm (decode share) + tensor (prefill share); the decode kernel runs on 9/16 of "
+             "the SMs while the prefill kernel starts on the rest, so its time alone (kernel "
+             "events) is longer than its share of the overlapped step",
     "long": "tensor",
     "long_w4096": "tensor",
     "long_d256": "tensor",

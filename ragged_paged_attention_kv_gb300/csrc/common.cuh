@@ -21,6 +21,7 @@ enum HeaderWord {
   kHdrDecodeChunk = 3,  // keys per decode split
   kHdrDecodeNext = 4,   // dynamic scheduler counter (decode)
   kHdrPrefillNext = 5,  // dynamic scheduler counter (prefill)
+  kHdrDecodeShare = 6,  // 1: the decode kernel leaves part of the SMs to the prefill kernel
   kHdrWords = 64,
 };
 

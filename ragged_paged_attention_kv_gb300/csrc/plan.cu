@@ -19,6 +19,18 @@ namespace rpa {
 
 constexpr int kSizeClasses = 16;  // decode sequences are ordered by these, longest first
 
+// A batch with both kinds of work runs its decode units on part of the SMs
+// (the decode kernel's CTAs on the other SMs leave at once) and the prefill
+// kernel's CTAs, launched behind it and waiting for no part of it, on the
+// rest from the start: the decode stays HBM-bound on fewer SMs (measured on
+// GB300: 9/16 of the SMs keep about 80 % of its bandwidth) while the prefill
+// is bound by the tensor cores.  Only worth it when the prefill is big enough
+// to keep the freed SMs busy: at least kShareFlopsPerByte prefill flops per
+// byte of keys / values the decode reads (the chunked-prefill mixed batch has
+// about 140, the fp8 windowed batch about 60; a small chunk beside a decode
+// batch well under 1).
+constexpr double kShareFlopsPerByte = 32.0;
+
 // Block-wide exclusive scan of two ints per thread (one set of barriers for
 // both); returns the prefixes and writes the block totals to *total.  All
 // threads of the block must call it.
@@ -116,7 +128,7 @@ __global__ void __launch_bounds__(kT) plan_kernel(rpa_params_t p, const int32_t*
                                                             int prefill_rows) {
   __shared__ int s_flags;
   __shared__ int2 s_scan[33];
-  __shared__ unsigned long long s_keys;
+  __shared__ unsigned long long s_keys, s_pairs;
   constexpr int kWarps = kT / 32;
   static_assert((kSizeClasses + 1) * kWarps <= kT, "one scan covers the class counts");
   __shared__ int s_doff[kT], s_poff[kT], s_nsplit[kT], s_ntiles[kT], s_lo[kT], s_len[kT],
@@ -142,6 +154,7 @@ __global__ void __launch_bounds__(kT) plan_kernel(rpa_params_t p, const int32_t*
   if (tid == 0) {
     s_flags = 0;
     s_keys = 0ull;
+    s_pairs = 0ull;
     s_maxkey = 0;
   }
   __syncthreads();
@@ -162,7 +175,8 @@ __global__ void __launch_bounds__(kT) plan_kernel(rpa_params_t p, const int32_t*
   }
 
   // Pass 1: total decode keys (per kv head) to size the splits.
-  unsigned long long my_keys = 0;
+  // ... and the prefill's (query token, visible key) pairs, for the SM share
+  unsigned long long my_keys = 0, my_pairs = 0;
   int my_max = 0;
   for (int s = tid; s < S; s += kT) {
     SeqPlan sp = classify(p, s, d0, s == tid ? meta0 : load_meta(s, kv_lens, qsl));
@@ -171,13 +185,28 @@ __global__ void __launch_bounds__(kT) plan_kernel(rpa_params_t p, const int32_t*
       my_keys += (unsigned long long)(sp.kv_len - sp.lo);
       my_max = max(my_max, sp.kv_len - sp.lo);
     }
+    if (sp.cls == 2) {
+      // token i sees min(ctx + i + 1, W) keys: sum over k = a .. b of min(k, W)
+      const unsigned long long a = (unsigned long long)(sp.kv_len - sp.q_len) + 1, b = sp.kv_len;
+      const unsigned long long w = p.sliding_window > 0 ? (unsigned long long)p.sliding_window : b;
+      if (w >= b)
+        my_pairs += (a + b) * (b - a + 1) / 2;
+      else if (w < a)
+        my_pairs += (b - a + 1) * w;
+      else
+        my_pairs += (a + w) * (w - a + 1) / 2 + (b - w) * w;
+    }
   }
   my_max = __reduce_max_sync(0xffffffffu, my_max);
   if ((tid & 31) == 0 && my_max) atomicMax(&s_maxkey, my_max);
   // warp sums first: one shared atomic per warp, not per thread
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) my_keys += __shfl_xor_sync(0xffffffffu, my_keys, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    my_keys += __shfl_xor_sync(0xffffffffu, my_keys, o);
+    my_pairs += __shfl_xor_sync(0xffffffffu, my_pairs, o);
+  }
   if ((tid & 31) == 0 && my_keys) atomicAdd(&s_keys, my_keys);
+  if ((tid & 31) == 0 && my_pairs) atomicAdd(&s_pairs, my_pairs);
   __syncthreads();
   const unsigned long long want =
       (s_keys * (unsigned long long)Hkv + kDecodeUnitsTarget - 1) / kDecodeUnitsTarget;
@@ -280,6 +309,11 @@ __global__ void __launch_bounds__(kT) plan_kernel(rpa_params_t p, const int32_t*
     ws[kHdrDecodeChunk] = chunk;
     ws[kHdrDecodeNext] = 0;
     ws[kHdrPrefillNext] = 0;
+    const double dec_bytes = (double)s_keys * Hkv * 2.0 * p.head_dim *
+                             (p.kv_dtype == RPA_KV_FP8_E4M3 ? 1.0 : 2.0);
+    const double pf_flops = (double)s_pairs * 4.0 * p.head_dim * p.num_q_heads;
+    ws[kHdrDecodeShare] =
+        dec_base > 0 && pf_base > 0 && pf_flops >= kShareFlopsPerByte * dec_bytes ? 1 : 0;
   }
 }
 
