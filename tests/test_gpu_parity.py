@@ -431,6 +431,47 @@ def test_many_units_with_ragged_tails(name, make):
     check_case(make())
 
 
+# The planner lets the decode kernel leave part of the SMs to the prefill
+# kernel when the prefill's flops reach 32 per byte of keys/values the decode
+# reads (header word 6 of the workspace).  Both sides of that decision, with
+# parity: a few decode sequences beside a large prefill (shared), and many
+# decode sequences beside a short chunk (not shared).
+SHARE_CASES = [
+    ("shared_bf16", True, lambda: _case("sh1", 911, [1] * 6 + [700, 300],
+                                        [300, 41, 1000, 77, 129, 640, 900, 300],
+                                        num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                        distribution=[6, 6, 8])),
+    ("shared_fp8_window", True, lambda: _case("sh2", 912, [1] * 40 + [256] * 3,
+                                              [200 + 37 * i for i in range(40)] + [900, 400, 256],
+                                              num_q_heads=64, num_kv_heads=8, head_dim=64,
+                                              kv_dtype="fp8", k_scale=0.05, v_scale=0.05,
+                                              sliding_window=128, logits_soft_cap=30.0,
+                                              has_sink=True, distribution=[40, 43, 43])),
+    ("not_shared", False, lambda: _case("sh3", 913, [1] * 64 + [4],
+                                        [2000 + 13 * i for i in range(64)] + [100],
+                                        num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                        distribution=[64, 65, 65])),
+]
+
+
+@pytest.mark.parametrize("name,shared,make", SHARE_CASES, ids=[c[0] for c in SHARE_CASES])
+def test_decode_and_prefill_share_the_sms(name, shared, make):
+    w = make()
+    q, k, v = w.make_qkv()
+    pool = w.make_pool("cpu")
+    sink = w.make_sink()
+    ref_out, ref_cache = run_oracle(w, q, k, v, pool, sink)
+    params = rpa.make_params(**{k_: v_ for k_, v_ in w.params().items()
+                                if k_ not in ("kv_fp8", "k_scale_heads", "v_scale_heads")},
+                             kv_fp8=w.kv_dtype == "fp8")
+    ws = rpa.alloc_workspace(params, DEV)
+    out, pool_after, status = run_gpu(w, q, k, v, pool, sink, workspace=ws)
+    assert status == 0, f"status {status:#x}"
+    assert int(ws[:32].view(torch.int32)[6].item()) == int(shared)
+    assert np.array_equal(pool_bytes(pool_after), ref_cache)
+    assert_close(out[:w.num_query_tokens], ref_out, name)
+
+
 def test_decode_split_boundaries():
     # kv lengths at page and split boundaries, all decode, big enough batch that
     # the planner's split size stays at its minimum
