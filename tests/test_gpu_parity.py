@@ -543,9 +543,14 @@ def _status_of(w, mutate):
     return status, out, pool, pool_after
 
 
-def test_bad_page_sets_status_without_fault():
+# the e4m3 cases also run the page write ahead of the prefill, which reads the
+# metadata alongside the planner and must skip what the planner rejects
+_KV = {"bf16": {}, "fp8": dict(kv_dtype="fp8", k_scale=0.05, v_scale=0.05)}
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_bad_page_sets_status_without_fault(kv):
     from ragged_paged_attention_kv_gb300 import _lib
-    w = _case("bp", 131, [1, 4], [40, 30])
+    w = _case("bp", 131, [1, 4], [40, 30], **_KV[kv])
 
     def mutate(w):
         w.block_tables = w.block_tables.copy()
@@ -555,9 +560,10 @@ def test_bad_page_sets_status_without_fault():
     assert status & _lib.RPA_STATUS_BAD_PAGE
 
 
-def test_bad_kv_len_and_qsl_skip_sequence():
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_bad_kv_len_and_qsl_skip_sequence(kv):
     from ragged_paged_attention_kv_gb300 import _lib
-    w = _case("bk", 132, [1, 4, 3], [40, 30, 9])
+    w = _case("bk", 132, [1, 4, 3], [40, 30, 9], **_KV[kv])
 
     def mutate(w):
         w.kv_lens_valid = w.kv_lens_valid.copy()
@@ -566,11 +572,20 @@ def test_bad_kv_len_and_qsl_skip_sequence():
     assert status == _lib.RPA_STATUS_BAD_KV_LEN
     qsl = w.query_start_loc
     assert np.all(out[qsl[1]:qsl[2]] == 7.0)  # the skipped sequence's rows untouched
+    # ... and its pages: only the other sequences' new-token slots change
+    rows = w.num_pages * w.page_size
+    got = pool_bytes(pool_after).reshape(rows, -1)
+    before = pool_bytes(pool).reshape(rows, -1)
+    pages = w.block_tables[w.pages_per_seq:w.pages_per_seq + 2]  # its 30 keys' two pages
+    slots = (pages[:, None].astype(np.int64) * w.page_size + np.arange(w.page_size)).ravel()
+    slots = slots[(slots >= 0) & (slots < rows)]
+    assert np.array_equal(got[slots], before[slots])
 
 
-def test_bad_distribution_plans_nothing():
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_bad_distribution_plans_nothing(kv):
     from ragged_paged_attention_kv_gb300 import _lib
-    w = _case("bd", 133, [1, 4], [40, 30])
+    w = _case("bd", 133, [1, 4], [40, 30], **_KV[kv])
 
     def mutate(w):
         w.distribution = np.array([2, 1, 2], np.int32)
