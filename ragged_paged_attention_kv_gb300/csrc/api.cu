@@ -84,9 +84,9 @@ int enqueue_forward(const rpa_params_t& p, const AttnArgs& a, const int32_t* dis
   if (launch_plan(p, a.kv_lens, a.qsl, distribution, a.kv.ws, prefill_rows_for(p), s) !=
       cudaSuccess)
     return RPA_ERR_CUDA;
-  // e4m3 cache, head_dim 64/128 tcgen05 prefill: that kernel reads the step's
-  // new tokens from their pages, written here once (timed with the planner)
-  if (kind == kPrefillTc && p.kv_dtype == RPA_KV_FP8_E4M3 &&
+  // e4m3 cache, tcgen05 prefills: they read the step's new tokens from their
+  // pages, written here once (timed with the planner)
+  if (kind != kPrefillMma && p.kv_dtype == RPA_KV_FP8_E4M3 &&
       launch_prefill_pages(a.kv, a.kv_lens, a.qsl, distribution, num_sms, s) != cudaSuccess)
     return RPA_ERR_CUDA;
   if (!mark(1)) return RPA_ERR_CUDA;

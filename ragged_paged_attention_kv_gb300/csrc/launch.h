@@ -12,9 +12,10 @@ cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int
                         const int32_t* dist, int32_t* ws, int prefill_rows, cudaStream_t stream);
 cudaError_t launch_cache_write(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,
                                int prefill_rows, int num_sms, cudaStream_t stream);
-// e4m3 cache with the head_dim 64/128 tcgen05 prefill: the new tokens of the
-// sequences the prefill kernel serves go into their pages ahead of the
-// attention kernels (launched right behind the planner, overlapping it).
+// e4m3 cache with a tcgen05 prefill (head_dim 64/128/192/256): the new
+// tokens of the sequences the prefill kernel serves go into their pages
+// ahead of the attention kernels (launched right behind the planner,
+// overlapping it).
 cudaError_t launch_prefill_pages(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,
                                  const int32_t* dist, int num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, int max_units, int num_sms, cudaStream_t stream);

@@ -361,8 +361,8 @@ cudaError_t launch_plan(const rpa_params_t& p, const int32_t* kv_lens, const int
   return cudaGetLastError();
 }
 
-// Page write ahead of the attention kernels (e4m3 cache, head_dim 64/128
-// tcgen05 prefill).  The new tokens of every sequence the planner gives to
+// Page write ahead of the attention kernels (e4m3 cache, tcgen05 prefills:
+// head_dim 64/128/192/256).  The new tokens of every sequence the planner gives to
 // the prefill kernel -- the planner's own classification, on the same
 // metadata -- are quantised into their pages once, so that kernel reads every
 // key and value tile from the pool as codes and no unit quantises a tile of
@@ -448,9 +448,19 @@ cudaError_t launch_prefill_pages(const KvArgs& a, const int32_t* kv_lens, const 
   const int T = a.p.total_tokens > 0 ? a.p.total_tokens : 1;
   int grid = (T + 7) / 8;  // at least one token per warp
   if (grid > 2 * num_sms) grid = 2 * num_sms;
-  if (a.p.head_dim == 64)
-    return launch_dependent(prefill_pages_kernel<64>, grid, 256, 0, stream, a, kv_lens, qsl, dist);
-  return launch_dependent(prefill_pages_kernel<128>, grid, 256, 0, stream, a, kv_lens, qsl, dist);
+  switch (a.p.head_dim) {
+    case 64:
+      return launch_dependent(prefill_pages_kernel<64>, grid, 256, 0, stream, a, kv_lens, qsl, dist);
+    case 128:
+      return launch_dependent(prefill_pages_kernel<128>, grid, 256, 0, stream, a, kv_lens, qsl,
+                              dist);
+    case 192:
+      return launch_dependent(prefill_pages_kernel<192>, grid, 256, 0, stream, a, kv_lens, qsl,
+                              dist);
+    default:
+      return launch_dependent(prefill_pages_kernel<256>, grid, 256, 0, stream, a, kv_lens, qsl,
+                              dist);
+  }
 }
 
 cudaError_t launch_cache_write(const KvArgs& a, const int32_t* kv_lens, const int32_t* qsl,

@@ -93,18 +93,19 @@ struct Maps {
 };
 
 // Geometry of one unit, computed identically by every role: key tiles of
-// 64, cached ones from c_start = lo rounded down to 64 up to ctx, then new
-// ones aligned to ctx.
+// 64, from the pool from c_start = lo rounded down to 64 up to k_end (= ctx,
+// or with an e4m3 cache the unit's last position + 1: the step's new tokens
+// are already in their pages), then new ones from the inputs aligned to ctx.
 struct Geom {
   int seq, h, q0, q_len, kv_len, ctx, t_begin, t_end;
   int lo;  // first key any row of the unit may see
-  int c_start, n_cached, i0, n_tiles;
+  int c_start, k_end, n_cached, i0, n_tiles;
   __device__ int lead(int key0) const { return lo > key0 ? lo - key0 : 0; }
   __device__ void tile(int j, bool& is_new, int& key0, int& valid) const {
     if (j < n_cached) {
       is_new = false;
       key0 = c_start + kN * j;
-      valid = min(kN, ctx - key0);
+      valid = min(kN, k_end - key0);
     } else {
       is_new = true;
       key0 = ctx + kN * (i0 + j - n_cached);
@@ -113,6 +114,7 @@ struct Geom {
   }
 };
 
+template <bool FROM_PAGES>
 __device__ __forceinline__ Geom unit_geom(const AttnArgs& a, const PrefillUnit& pu) {
   Geom g;
   g.seq = pu.seq;
@@ -126,16 +128,17 @@ __device__ __forceinline__ Geom unit_geom(const AttnArgs& a, const PrefillUnit& 
   const int W = a.kv.p.sliding_window;
   const int pos_first = g.ctx + g.t_begin, pos_last = g.ctx + g.t_end - 1;
   g.lo = (W > 0 && pos_first - W + 1 > 0) ? pos_first - W + 1 : 0;
-  if (g.lo < g.ctx) {
+  g.k_end = FROM_PAGES ? pos_last + 1 : g.ctx;
+  if (g.lo < g.k_end) {
     g.c_start = g.lo & ~(kN - 1);
-    g.n_cached = (g.ctx - g.c_start + kN - 1) / kN;
+    g.n_cached = (g.k_end - g.c_start + kN - 1) / kN;
   } else {
     g.c_start = 0;
     g.n_cached = 0;
   }
   g.i0 = g.lo > g.ctx ? (g.lo - g.ctx) / kN : 0;
   const int i1 = (pos_last - g.ctx) / kN;
-  g.n_tiles = g.n_cached + (i1 - g.i0 + 1);
+  g.n_tiles = g.n_cached + (FROM_PAGES ? 0 : i1 - g.i0 + 1);
   return g;
 }
 
@@ -216,19 +219,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool has_cap = p.logits_soft_cap > 0.f;
   const LogitXform xf0 = make_xform(p.softmax_scale, qk_scale(p, p.k_scale), p.logits_soft_cap);
 
-  // fp8 cache: decoding of a landed operand of tile j (staged codes, or for
-  // new rows the bf16 inputs quantised in place so they carry the codes the
-  // page write stores) into its operand stage, shared by kDecWarps warps.
-  // Value rows no row of the unit may see (past the valid range, or before
-  // the window) become zero; key rows there are masked by the softmax.
+  // fp8 cache: decoding of a landed operand of tile j (the staged codes:
+  // every tile of an e4m3 unit comes from the pages, the step's new tokens
+  // were written there ahead of this kernel) into its operand stage, shared
+  // by kDecWarps warps.  Value rows no row of the unit may see (past the
+  // valid range, or before the window) become zero; key rows there are
+  // masked by the softmax.
   auto decode_fp8 = [&](const Geom& g, uint32_t tc, int j, int kv, int part) {
     bool is_new;
     int key0, valid;
     g.tile(j, is_new, key0, valid);
     uint8_t* op = smem + (kv ? C::kOffV : C::kOffK) + (tc & 1) * kOperand;
     const uint8_t* stg = smem + C::kOffStg + kv * C::kStaging;
-    const float scale = !PH ? (kv ? p.v_scale : p.k_scale)
-                            : (kv ? v_scale_of(p, g.h) : k_scale_of(p, g.h));
     const int rows = kv ? kN : valid;
     const int lead = kv ? g.lead(key0) : 0;
     for (int idx = 32 * part + lane; idx < rows * (D / 8); idx += 32 * kDecWarps) {
@@ -237,8 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r >= valid || r < lead) {
         *dst = make_uint4(0, 0, 0, 0);
       } else {
-        const uint2 codes = is_new ? quantize8(*dst, scale)
-                                   : *reinterpret_cast<const uint2*>(stg + r * D + c * 8);
+        const uint2 codes = *reinterpret_cast<const uint2*>(stg + r * D + c * 8);
         *dst = kv ? dequant8_f16(codes) : dequant8(codes);
       }
     }
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       const int u = s_unit;
       if (u >= n_units || s_abort) break;
-      const Geom g = unit_geom(a, units[u]);
+      const Geom g = unit_geom<FP8>(a, units[u]);
       body(g, tcount, ucount);
       tcount += g.n_tiles;
       ucount += 1;
@@ -545,7 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // this unit's new tokens -> their pages, a quarter of them per warp
-      {
+      // (an e4m3 cache had them written ahead of this kernel)
+      if constexpr (!FP8) {
         const int n = g.t_end - g.t_begin, w = warp - 4;
         const int i0 = n * w / 4, i1 = n * (w + 1) / 4;
         write_tokens_kv<FP8, D, 2>(a.kv, g.seq, g.q0 + g.t_begin + i0, g.ctx + g.t_begin + i0,
