@@ -267,6 +267,14 @@ def prefill_kernel_name(w):
     return "prefill_kernel", "prefill.cu"
 
 
+def launches_per_step(w):
+    """The library's kernels one rpa_forward launches: planner, decode and
+    prefill kernels, and with an e4m3 cache and a tcgen05 prefill the page
+    write of the prefill sequences' new tokens."""
+    name, _ = prefill_kernel_name(w)
+    return 3 + (1 if w.kv_dtype == "fp8" and name != "prefill_kernel" else 0)
+
+
 # How each workload is bounded (the roofline each of its kernels is held to).
 BOUNDS = {
     "decode": "hbm",
@@ -517,7 +525,7 @@ def gpu_arm(args, world, rank, local):
         "decode_kv_gbs": head["decode_kv_gbs"],
         "prefill_tflops": head["prefill_tflops"],
         "e2e": head["e2e"],
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": head["clocks"],
     }
     if configs:
