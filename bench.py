@@ -367,7 +367,7 @@ def time_steps(ctx, steps, warmup, flush, stream, world, rank, dev):
 
     def events(n, k):
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(k)] for _ in range(n)]
-        for ev in evs:  # create the driver events before they are handed over
+        for ev in evs:  # record once so each CUDA event exists before its handle is passed on
             for e in ev:
                 e.record(stream)
         return evs
