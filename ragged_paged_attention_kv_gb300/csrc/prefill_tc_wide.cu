@@ -30,7 +30,11 @@
 // tokens are written into their pages by the softmax warps.  With an e4m3
 // cache the pages' codes land in a staging buffer and are decoded into the
 // operand stage: keys as bf16 (the queries' type), values as fp16 (exact for
-// e4m3), with P packed as fp16 to match.
+// e4m3), with P packed as fp16 to match.  With quantised queries (q_scale)
+// S = Q K^T runs on the e4m3 codes themselves (tcgen05.mma kind::f8f6f4):
+// the query tile is quantised once per unit into a code tile, key pages land
+// as codes in code-tile key stages, and the logit scale carries
+// q_scale * k_scale.
 #include "async.cuh"
 #include "common.cuh"
 #include "kv_write.cuh"
@@ -53,20 +57,37 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = 256;    // S slot b at kTmemS + 64 b
 constexpr int kRescaleLog2 = 8;
 
-template <int D, bool FP8>
+// With quantised queries (Q8) the query tile and the key stages are e4m3 code
+// tiles in blocks of 64 bytes (D/64 per row, 64-byte swizzle): the query
+// code tile [D/64][128 rows][64 B] and key stages [D/64][64 rows][64 B]; only
+// the values are staged.
+template <int D, bool FP8, bool Q8 = false>
 struct Cfg {
+  static_assert(!Q8 || FP8, "quantised queries need an e4m3 cache");
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kQBytes = kHalves * kHalfQ;
-  static constexpr uint32_t kOperand = kHalves * kHalfKV;  // one key or value stage
+  static constexpr uint32_t kOperand = kHalves * kHalfKV;  // one bf16 / fp16 operand stage
   static constexpr uint32_t kStaging = FP8 ? (uint32_t)kN * D : 0u;  // e4m3 codes of a tile
+  static constexpr uint32_t kBlkQ = 128 * 64, kBlkK = kN * 64;  // one 64-byte block of codes
+  static constexpr uint32_t kKStage = Q8 ? (uint32_t)kN * D : kOperand;  // key stage stride
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kQBytes;                // key stage s at kOffK + s*kOperand
-  static constexpr uint32_t kOffV = kQBytes + 2 * kOperand;  // value stage s
-  static constexpr uint32_t kOffStg = kQBytes + 4 * kOperand;  // staging kv at + kv*kStaging
-  static constexpr uint32_t kOffBar = (kOffStg + 2 * kStaging + 1023) / 1024 * 1024;
+  static constexpr uint32_t kOffQ8 = kQBytes;                          // Q8: query codes
+  static constexpr uint32_t kOffK = kQBytes + (Q8 ? 128u * D : 0u);    // + s*kKStage
+  static constexpr uint32_t kOffV = kOffK + 2 * kKStage;               // + s*kOperand
+  static constexpr uint32_t kOffStg = kOffV + 2 * kOperand;  // staging kv at + kv*kStaging
+  static constexpr int kStgOps = Q8 ? 1 : 2;                  // (Q8: values only, at kv 0)
+  static constexpr uint32_t kOffBar = (kOffStg + kStgOps * kStaging + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = (int)kOffBar + 256 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "fits one CTA's shared memory");
 };
+
+// Byte offset of the codes of elements 8*c8 .. 8*c8+7 of row r in a 64-byte
+// block of an e4m3 code tile (64-byte swizzle: 16-byte chunk XOR address
+// bits 7-8).
+__device__ __forceinline__ uint32_t sw64_codes(int r, int c8) {
+  return (uint32_t)r * 64 + (((((uint32_t)c8 & 7u) >> 1) ^ ((uint32_t)(r >> 1) & 3u)) << 4) +
+         ((uint32_t)(c8 & 1) << 3);
+}
 
 enum Bar {
   kBarQFull = 0,    // the query tile landed
@@ -90,6 +111,7 @@ struct Maps {
   CUtensorMap cache;  // pool [num_pages*P][2*Hkv][D], box {64, 1, min(P,64)} (fp8: {D, 1, ..})
   CUtensorMap knew;   // keys [T][Hkv][D], box {64, 1, 64}
   CUtensorMap vnew;   // values [T][Hkv][D], box {64, 1, 64}
+  CUtensorMap cache8; // Q8 only: the pool's codes, box {64, 1, min(P,64)}, 64-byte swizzle
 };
 
 // Geometry of one unit, computed identically by every role: key tiles of
@@ -142,10 +164,10 @@ __device__ __forceinline__ Geom unit_geom(const AttnArgs& a, const PrefillUnit& 
   return g;
 }
 
-template <int D, bool FP8, bool PH>
+template <int D, bool FP8, bool PH, bool Q8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_wide_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
-  using C = Cfg<D, FP8>;
+  using C = Cfg<D, FP8, Q8>;
   constexpr int kDecWarps = FP8 ? 3 : 1;  // warps that decode fp8 operands
   constexpr uint32_t kOperand = C::kOperand;
   extern __shared__ uint8_t smem_raw[];
@@ -207,13 +229,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&maps.cache);
     prefetch_tensormap(&maps.knew);
     prefetch_tensormap(&maps.vnew);
+    if (Q8) prefetch_tensormap(&maps.cache8);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  const uint32_t idesc_qk = idesc_bf16(kM, kN, false, false);
+  const uint32_t idesc_qk = Q8 ? idesc_e4m3(kM, kN) : idesc_bf16(kM, kN, false, false);
   // P and the values are fp16 with an e4m3 cache, bf16 otherwise
   const uint32_t idesc_pv = idesc_bf16(kM, D, false, true, FP8);
   const bool has_cap = p.logits_soft_cap > 0.f;
@@ -226,11 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // valid range, or before the window) become zero; key rows there are
   // masked by the softmax.
   auto decode_fp8 = [&](const Geom& g, uint32_t tc, int j, int kv, int part) {
+    if (Q8 && kv == 0) return;  // the key codes landed in their stage as they are
     bool is_new;
     int key0, valid;
     g.tile(j, is_new, key0, valid);
-    uint8_t* op = smem + (kv ? C::kOffV : C::kOffK) + (tc & 1) * kOperand;
-    const uint8_t* stg = smem + C::kOffStg + kv * C::kStaging;
+    uint8_t* op = smem + (kv ? C::kOffV + (tc & 1) * kOperand : C::kOffK + (tc & 1) * C::kKStage);
+    const uint8_t* stg = smem + C::kOffStg + (Q8 ? 0 : kv) * C::kStaging;
     const int rows = kv ? kN : valid;
     const int lead = kv ? g.lead(key0) : 0;
     for (int idx = 32 * part + lane; idx < rows * (D / 8); idx += 32 * kDecWarps) {
@@ -298,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool is_new;
         int key0, valid;
         g.tile(j, is_new, key0, valid);
-        const uint32_t dst = sb + (kv ? C::kOffV : C::kOffK) + s * kOperand;
+        const uint32_t dst = sb + (kv ? C::kOffV + s * kOperand : C::kOffK + s * C::kKStage);
         const uint32_t fullbar = bar((kv ? kBarVFull : kBarKFull) + s);
         if (is_new) {
           if (lane == 0) {
@@ -321,9 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int srow = P < kN ? (pg0 + lane) * P - key0 : 0;
             const int z = page * P + (P < kN ? 0 : key0 % P);
-            if (FP8) {
-              tma_load_3d(sb + C::kOffStg + kv * C::kStaging + srow * D, &maps.cache, fullbar, 0,
-                          2 * g.h + kv, z);
+            if (Q8 && kv == 0) {
+              for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_load_3d(dst + hf * C::kBlkK + srow * 64, &maps.cache8, fullbar, hf * 64, 2 * g.h,
+                            z);
+            } else if (FP8) {
+              tma_load_3d(sb + C::kOffStg + (Q8 ? 0 : kv) * C::kStaging + srow * D, &maps.cache,
+                          fullbar, 0, 2 * g.h + kv, z);
             } else {
               for (int hf = 0; hf < C::kHalves; ++hf)
                 tma_load_3d(dst + hf * kHalfKV + srow * 128, &maps.cache, fullbar, hf * 64,
@@ -433,21 +461,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S(0), S(1), then per tile j: P V(j), S(j+2).  Key stage and S slot
       // of tile j are both (tcount + j) & 1.
       if (lane == 0) {
-        bool ok = mbar_wait(bar(FP8 && p.q_scale > 0.f ? kBarQReady : kBarQFull), ucount & 1,
-                            &s_abort);
+        bool ok = mbar_wait(bar(Q8 ? kBarQReady : kBarQFull), ucount & 1, &s_abort);
         tc_fence_after();
         auto qk = [&](uint32_t tc) -> bool {
           const int s = tc & 1;
           if (!mbar_wait(bar((FP8 ? kBarKReady : kBarKFull) + s), (tc >> 1) & 1, &s_abort))
             return false;
           tc_fence_after();
-          const uint32_t sK = sb + C::kOffK + s * kOperand;
-          const uint32_t sQ = sb + C::kOffQ;
-          for (int k = 0; k < D / 16; ++k) {
-            umma_ss(tmem + kTmemS + 64 * s,
-                    sdesc_sw128(sQ + (k >> 2) * kHalfQ + (k & 3) * 32, 16, 1024),
-                    sdesc_sw128(sK + (k >> 2) * kHalfKV + (k & 3) * 32, 16, 1024), idesc_qk,
-                    k > 0 ? 1u : 0u);
+          const uint32_t sK = sb + C::kOffK + s * C::kKStage;
+          if constexpr (Q8) {
+            // e4m3 codes: 32 per product, two products per 64-byte block
+            const uint32_t sQ = sb + C::kOffQ8;
+            for (int k = 0; k < D / 32; ++k) {
+              const uint32_t off = (uint32_t)(k & 1) * 32;
+              umma_ss_e4m3(tmem + kTmemS + 64 * s,
+                           sdesc_sw64(sQ + (k >> 1) * C::kBlkQ + off, 16, 512),
+                           sdesc_sw64(sK + (k >> 1) * C::kBlkK + off, 16, 512), idesc_qk,
+                           k > 0 ? 1u : 0u);
+            }
+          } else {
+            const uint32_t sQ = sb + C::kOffQ;
+            for (int k = 0; k < D / 16; ++k) {
+              umma_ss(tmem + kTmemS + 64 * s,
+                      sdesc_sw128(sQ + (k >> 2) * kHalfQ + (k & 3) * 32, 16, 1024),
+                      sdesc_sw128(sK + (k >> 2) * kHalfKV + (k & 3) * 32, 16, 1024), idesc_qk,
+                      k > 0 ? 1u : 0u);
+            }
           }
           umma_commit(bar(kBarSFull + s));
           umma_commit(bar(kBarKEmpty + s));
@@ -527,10 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = g.ctx + i_tok;
       const int hq = g.h * G + r % G;
       const uint32_t tO = tmem + lane_off + kTmemO;
-      if (FP8 && p.q_scale > 0.f) {  // q_scale needs an e4m3 cache
-        // quantised queries: the four softmax warps turn the query tile into
-        // its e4m3 codes' values (element by element, in place) before the
-        // MMA thread reads it
+      if constexpr (Q8) {
+        // quantised queries: the four softmax warps turn the bf16 query tile
+        // into its e4m3 code tile (q / q_scale rounded to e4m3) before the MMA
+        // thread reads it
         if (!mbar_wait_warp(bar(kBarQFull), ucount & 1, &s_abort)) {
           if (lane == 0) {
             set_status(hdr, RPA_STATUS_TIMEOUT);
@@ -538,8 +577,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           return;
         }
-        uint4* qt = reinterpret_cast<uint4*>(smem + C::kOffQ);
-        for (int i = tid - 128; i < (int)(C::kQBytes / 16); i += 128) quantize_q8(qt + i, p.q_scale);
+        constexpr int kChunks = D / 8;  // 8 elements per chunk
+        for (int i = tid - 128; i < kM * kChunks; i += 128) {
+          const int rr = i / kChunks, c = i % kChunks;
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + C::kOffQ + (c >> 3) * kHalfQ +
+                                                          sw128(rr, c & 7));
+          *reinterpret_cast<uint2*>(smem + C::kOffQ8 + (c >> 3) * C::kBlkQ + sw64_codes(rr, c)) =
+              quantize8(v, p.q_scale);
+        }
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarQReady));
@@ -697,28 +742,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace tcw
 
-template <int D, bool FP8, bool PH>
+template <int D, bool FP8, bool PH, bool Q8>
 static cudaError_t launch_wide_t(const AttnArgs& a, int max_units, int num_sms,
                                  cudaStream_t stream) {
-  using C = tcw::Cfg<D, FP8>;
+  using C = tcw::Cfg<D, FP8, Q8>;
   static std::atomic<unsigned long long> attr_done{0};
-  auto kern = tcw::prefill_tc_wide_kernel<D, FP8, PH>;
+  auto kern = tcw::prefill_tc_wide_kernel<D, FP8, PH, Q8>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes, &attr_done);
   if (e != cudaSuccess) return e;
   const rpa_params_t& p = a.kv.p;
   const int G = p.num_q_heads / p.num_kv_heads;
-  tcw::Maps maps;
+  tcw::Maps maps{};
   const uint64_t T = (uint64_t)(p.total_tokens > 0 ? p.total_tokens : 1);
+  const uint64_t rows = (uint64_t)p.num_pages * p.page_size;
   const uint32_t prow = p.page_size < tcw::kN ? (uint32_t)p.page_size : (uint32_t)tcw::kN;
   bool ok = encode_map_3d(&maps.q, a.queries, 2, D, (uint64_t)p.num_q_heads, T, 64u, (uint32_t)G,
                           (uint32_t)(tcw::kM / G), true) &&
             encode_map_3d(&maps.cache, a.kv.cache, FP8 ? 1 : 2, D, 2 * (uint64_t)p.num_kv_heads,
-                          (uint64_t)p.num_pages * p.page_size, FP8 ? (uint32_t)D : 64u, 1u, prow,
-                          !FP8) &&
+                          rows, FP8 ? (uint32_t)D : 64u, 1u, prow, !FP8) &&
             encode_map_3d(&maps.knew, a.kv.keys, 2, D, (uint64_t)p.num_kv_heads, T, 64u, 1u,
                           (uint32_t)tcw::kN, true) &&
             encode_map_3d(&maps.vnew, a.kv.values, 2, D, (uint64_t)p.num_kv_heads, T, 64u, 1u,
-                          (uint32_t)tcw::kN, true);
+                          (uint32_t)tcw::kN, true) &&
+            (!Q8 || encode_map_3d_swizzle(&maps.cache8, a.kv.cache, 1, D,
+                                          2 * (uint64_t)p.num_kv_heads, rows, 64u, 1u, prow, 64));
   if (!ok) return cudaErrorInvalidValue;
   int grid = num_sms;
   if (grid > max_units) grid = max_units;
@@ -726,17 +773,25 @@ static cudaError_t launch_wide_t(const AttnArgs& a, int max_units, int num_sms,
   return launch_dependent(kern, grid, tcw::kThreads, C::kSmemBytes, stream, maps, a);
 }
 
+template <int D>
+static cudaError_t launch_wide_d(const AttnArgs& a, int max_units, int num_sms,
+                                 cudaStream_t stream) {
+  const rpa_params_t& p = a.kv.p;
+  if (p.kv_dtype != RPA_KV_FP8_E4M3)
+    return launch_wide_t<D, false, false, false>(a, max_units, num_sms, stream);
+  // quantised queries (an e4m3 cache only) run Q K^T on the codes
+  const bool ph = p.k_scale_heads != nullptr || p.v_scale_heads != nullptr;
+  if (p.q_scale > 0.f)
+    return ph ? launch_wide_t<D, true, true, true>(a, max_units, num_sms, stream)
+              : launch_wide_t<D, true, false, true>(a, max_units, num_sms, stream);
+  return ph ? launch_wide_t<D, true, true, false>(a, max_units, num_sms, stream)
+            : launch_wide_t<D, true, false, false>(a, max_units, num_sms, stream);
+}
+
 cudaError_t launch_prefill_tc_wide(const AttnArgs& a, int max_units, int num_sms,
                                    cudaStream_t stream) {
-  const bool fp8 = a.kv.p.kv_dtype == RPA_KV_FP8_E4M3;
-  const bool ph = a.kv.p.k_scale_heads != nullptr || a.kv.p.v_scale_heads != nullptr;
-  if (a.kv.p.head_dim == 192)
-    return !fp8 ? launch_wide_t<192, false, false>(a, max_units, num_sms, stream)
-           : ph  ? launch_wide_t<192, true, true>(a, max_units, num_sms, stream)
-                 : launch_wide_t<192, true, false>(a, max_units, num_sms, stream);
-  return !fp8 ? launch_wide_t<256, false, false>(a, max_units, num_sms, stream)
-         : ph  ? launch_wide_t<256, true, true>(a, max_units, num_sms, stream)
-               : launch_wide_t<256, true, false>(a, max_units, num_sms, stream);
+  return a.kv.p.head_dim == 192 ? launch_wide_d<192>(a, max_units, num_sms, stream)
+                                : launch_wide_d<256>(a, max_units, num_sms, stream);
 }
 
 }  // namespace rpa

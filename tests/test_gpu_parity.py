@@ -279,6 +279,10 @@ POISON_CASES = [
                                                       kv_dtype="fp8", k_scale=0.3, v_scale=0.1,
                                                       q_scale=0.02, head_dim=128,
                                                       page_size=64, sliding_window=300)),
+    ("tcw_q8_d256_p8_window", lambda: _case("z19", 319, [1, 90, 33], [600, 500, 35],
+                                            kv_dtype="fp8", k_scale=0.3, v_scale=0.1,
+                                            q_scale=0.02, head_dim=256, num_q_heads=16,
+                                            num_kv_heads=8, page_size=8, sliding_window=150)),
     ("tc_q8_d64_options", lambda: _case("z18", 318, [1, 1, 64, 20], [900, 129, 200, 21],
                                         kv_dtype="fp8", k_scale=0.05, v_scale=0.07,
                                         q_scale=0.02, num_q_heads=64, num_kv_heads=8,
@@ -397,6 +401,12 @@ Q8_CASES = [
                                               [1000, 70, 600, 900], head_dim=64,
                                               num_q_heads=32, num_kv_heads=8, page_size=128,
                                               sliding_window=500)),
+    # the same on the head_dim 192/256 prefill (64-byte code blocks)
+    ("tcw_q8_d192_many_units", lambda: _q8("q14", 514, [70] * 10 + [3] * 30,
+                                           [300 + 41 * i for i in range(10)] +
+                                           [40 + 23 * i for i in range(30)],
+                                           head_dim=192, num_q_heads=16, num_kv_heads=4,
+                                           page_size=16, logits_soft_cap=25.0)),
 ]
 
 
