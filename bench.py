@@ -65,6 +65,8 @@ DESCRIPTIONS = {
                   "bf16, page_size 64",
     "long_small_fp8": "long_small with an e4m3 cache (k/v scale 0.05): 1 seq q=kv=8192 causal; "
                       "Hq32/Hkv8/D128, page_size 64 (profiling size)",
+    "long_small_fp8_w8a8": "long_small_fp8 with quantised queries (q_scale 0.02): Q K^T of the "
+                           "prefill on e4m3 codes (profiling size)",
     "fp8_small": "fp8 shape at profiling size: 64 decode + 8x256 chunks; e4m3 cache, cap 30, "
                  "sinks, window 128; Hq64/Hkv8/D64, page_size 16",
     "tiny": "tiny mixed batch: 3 seqs (1,17),(24,24),(5,40); Hq4/Hkv2/D64/P16",

@@ -422,9 +422,10 @@ def long_d256() -> Workload:
                     distribution=np.array([0, 0, 2], np.int32), total_tokens=2 * L)
 
 
-def long_small(kv_dtype: str = "bf16", name: str = "long_small") -> Workload:
+def long_small(kv_dtype: str = "bf16", name: str = "long_small", q_scale: float = 0.0) -> Workload:
     """The long-context shape at one sequence of 8192 tokens (profiling size);
-    with kv_dtype "fp8" the same prefill into an e4m3 cache (k/v scale 0.05)."""
+    with kv_dtype "fp8" the same prefill into an e4m3 cache (k/v scale 0.05),
+    and with q_scale > 0 its queries quantised as well."""
     seed = 1014
     g = torch.Generator().manual_seed(seed)
     P, L = 64, 8192
@@ -439,7 +440,7 @@ def long_small(kv_dtype: str = "bf16", name: str = "long_small") -> Workload:
                     logits_soft_cap=0.0, k_scale=0.05 if fp8 else 1.0,
                     v_scale=0.05 if fp8 else 1.0, has_sink=False,
                     q_lens=q, kv_lens_valid=kv, block_tables=bt,
-                    distribution=np.array([0, 0, 1], np.int32), total_tokens=L)
+                    distribution=np.array([0, 0, 1], np.int32), total_tokens=L, q_scale=q_scale)
 
 
 def fp8(q_scale: float = 0.0, name: str = "fp8") -> Workload:
@@ -496,6 +497,7 @@ WORKLOADS = {
     "long_w4096": lambda: long(4096),
     "long_small": long_small,
     "long_small_fp8": lambda: long_small("fp8", "long_small_fp8"),
+    "long_small_fp8_w8a8": lambda: long_small("fp8", "long_small_fp8_w8a8", 0.02),
     "fp8": fp8,
     # the fp8 batch with quantised queries: |q| of N(0,1) samples stays far
     # below 448 * 0.02, so no query code saturates
