@@ -638,9 +638,11 @@ def test_decode_units_fill_the_workspace_bound(head_dim):
         assert np.array_equal(again[:S], first), "decode output differs between runs"
 
 
-def test_empty_batch_is_a_no_op():
-    """distribution = [0, 0, 0]: no sequence, nothing planned, nothing written."""
-    w = _case("eb", 136, [1, 4], [40, 30], distribution=[0, 0, 0])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_empty_batch_is_a_no_op(kv):
+    """distribution = [0, 0, 0]: no sequence, nothing planned, nothing written
+    (with an e4m3 cache the page write ahead of the prefill runs too)."""
+    w = _case("eb", 136, [1, 4], [40, 30], distribution=[0, 0, 0], **_KV[kv])
     q, k, v = w.make_qkv()
     pool = w.make_pool("cpu")
     out, pool_after, status = run_gpu(w, q, k, v, pool)
