@@ -1,4 +1,5 @@
-// Planner and standalone page write.
+// Planner, the page write ahead of the prefill (e4m3 caches), and the
+// standalone page write.
 //
 // The planner reads the ragged metadata on the device (no host round trip),
 // checks it, and splits the batch into work units by class: sequences of the
@@ -7,7 +8,8 @@
 // (sequence, tile of new tokens, kv head) units.  The ejkernel
 // ragged_page_attention_v3 interface's `distribution` argument defines the
 // classes; results never depend on it (a decode-class sequence with
-// q_len != 1 is flagged and planned as a prefill).
+// q_len != 1 is flagged and planned as a prefill).  It also decides whether
+// the decode kernel leaves part of the SMs to the prefill kernel.
 #include <cfloat>
 
 #include "common.cuh"

@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (Q8) {
       // quantised queries: all eight softmax warps turn both bf16 query
       // tiles into e4m3 code tiles (q / q_scale rounded to e4m3) before the
-      // MMA thread reads them and new keys land over the bf16 tiles
+      // MMA thread reads them
       q_ok = mbar_wait_warp(bar(kBarQFull), ucount & 1, &s_abort);
       if (q_ok) {
         constexpr int kChunks = D / 8;  // 8 elements per chunk
