@@ -541,23 +541,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               return false;
             tc_fence_after();
           }
-          const uint32_t sK = sb + kOffK + s * C::kKStage;
+          const uint32_t sK = sb + kOffK + s * C::kKStage, dS = tmem + kTmemS + 128 * x;
+          // one thread issues every product: its descriptors are the tiles'
+          // (built once here) advanced by constants, so the issue keeps pace
+          // with the tensor core
           if constexpr (Q8) {
             // e4m3 codes, 32 per product along the row (rows of D bytes)
             const uint32_t sQ = sb + C::kOffQ8 + x * C::kTile8;
-            for (int k = 0; k < D / 32; ++k) {
-              const uint64_t ad = D == 128 ? sdesc_sw128(sQ + 32 * k, 16, 1024)
-                                           : sdesc_sw64(sQ + 32 * k, 16, 512);
-              const uint64_t bd = D == 128 ? sdesc_sw128(sK + 32 * k, 16, 1024)
-                                           : sdesc_sw64(sK + 32 * k, 16, 512);
-              umma_ss_e4m3(tmem + kTmemS + 128 * x, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
-            }
+            const uint64_t dq = D == 128 ? sdesc_sw128(sQ, 16, 1024) : sdesc_sw64(sQ, 16, 512);
+            const uint64_t dk = D == 128 ? sdesc_sw128(sK, 16, 1024) : sdesc_sw64(sK, 16, 512);
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k)
+              umma_ss_e4m3(dS, sdesc_advance(dq, 32 * k), sdesc_advance(dk, 32 * k), idesc_qk,
+                           k > 0 ? 1u : 0u);
           } else {
-            const uint32_t sQ = sb + kOffQ + x * kOperand;
+            const uint64_t dq = sdesc_sw128(sb + kOffQ + x * kOperand, 16, 1024),
+                           dk = sdesc_sw128(sK, 16, 1024);
+#pragma unroll
             for (int k = 0; k < D / 16; ++k) {
               const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-              umma_ss(tmem + kTmemS + 128 * x, sdesc_sw128(sQ + off, 16, 1024),
-                      sdesc_sw128(sK + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+              umma_ss(dS, sdesc_advance(dq, off), sdesc_advance(dk, off), idesc_qk,
+                      k > 0 ? 1u : 0u);
             }
           }
           umma_commit(bar(kBarSFull + x));
@@ -569,12 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar(kBarPReady + x), (n.tiles(x) + j) & 1, &s_abort)) return false;
           if (x == 0 && !mbar_wait(bar(kBarVReady + s), (tc >> 1) & 1, &s_abort)) return false;
           tc_fence_after();
-          const uint32_t sV = sb + kOffV + s * kOperand;
-          for (int k = 0; k < kN / 16; ++k) {
-            const uint64_t bd = sdesc_sw128(sV + k * 16 * 128, kHalf, 1024);
-            umma_ts(tmem + kTmemO + 128 * x, tmem + kTmemS + 128 * x + 8 * k, bd, idesc_pv,
+          const uint64_t dv = sdesc_sw128(sb + kOffV + s * kOperand, kHalf, 1024);
+          const uint32_t tO = tmem + kTmemO + 128 * x, tP = tmem + kTmemS + 128 * x;
+#pragma unroll
+          for (int k = 0; k < kN / 16; ++k)
+            umma_ts(tO, tP + 8 * k, sdesc_advance(dv, k * 16 * 128), idesc_pv,
                     (j > 0 || k > 0) ? 1u : 0u);
-          }
           if (last_of_stage) umma_commit(bar(kBarVEmpty + s));
           return true;
         };

@@ -401,11 +401,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(kBarVReady + s));
         return true;
       };
-      // Per tile j: keys of j, (fp8) decode keys of j-1, values of j, then
-      // finalize values of j-1.  With the one staging buffer per operand of
-      // an fp8 cache, the codes of tile j-1 are decoded (by every decoding
-      // warp) before those of tile j are fetched.
+      // bf16 cache: the keys run one tile ahead of the values.  S(j+2) is
+      // issued right after P V(j), so the keys of tile j+2 are fetched as
+      // soon as S(j) has freed their stage, not behind the values of tile
+      // j+1 (whose stage frees only with P V(j-1)).  Per step j: keys of j+1,
+      // values of j, then finalize values of j-1.
       bool ok = true;
+      if constexpr (!FP8) {
+        int ids_j = load_ids(0);
+        int ids_j1 = nt > 1 ? load_ids(1) : 0;
+        if (nt >= 1) {
+          if (!mbar_wait_warp(bar(kBarKEmpty + (tcount & 1)), ((tcount >> 1) & 1) ^ 1, &s_abort))
+            ok = false;
+          else {
+            issue(0, 0, tcount, ids_j);
+            ((tcount & 1) ? k_last1 : k_last0) = (int)tcount;
+          }
+        }
+        for (int j = 0; j < nt && ok; ++j) {
+          const uint32_t tc = tcount + j;
+          const int s = tc & 1;
+          if (j + 1 < nt) {
+            const uint32_t tn = tc + 1;
+            if (!mbar_wait_warp(bar(kBarKEmpty + (tn & 1)), ((tn >> 1) & 1) ^ 1, &s_abort)) {
+              ok = false;
+              break;
+            }
+            issue(j + 1, 0, tn, ids_j1);
+            ((tn & 1) ? k_last1 : k_last0) = (int)tn;
+          }
+          const int ids_j2 = j + 2 < nt ? load_ids(j + 2) : 0;
+          if (!mbar_wait_warp(bar(kBarVEmpty + s), ((tc >> 1) & 1) ^ 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          issue(j, 1, tc, ids_j);
+          (s ? v_last1 : v_last0) = (int)tc;
+          __syncwarp();
+          if (j >= 1) ok = finalize_v(tc - 1, j - 1);
+          ids_j = ids_j1;
+          ids_j1 = ids_j2;
+        }
+        if (ok && nt >= 1) ok = finalize_v(tcount + nt - 1, nt - 1);
+        if (!ok && lane == 0) {
+          set_status(hdr, RPA_STATUS_TIMEOUT);
+          s_abort = 1;
+        }
+        return;
+      }
+      // e4m3 cache, per tile j: keys of j, decode keys of j-1, values of j,
+      // then finalize values of j-1.  With the one staging buffer per
+      // operand, the codes of tile j-1 are decoded (by every decoding warp)
+      // before those of tile j are fetched.
       int ids_next = load_ids(0);
       for (int j = 0; j < nt && ok; ++j) {
         const uint32_t tc = tcount + j;
@@ -470,23 +517,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar((FP8 ? kBarKReady : kBarKFull) + s), (tc >> 1) & 1, &s_abort))
             return false;
           tc_fence_after();
-          const uint32_t sK = sb + C::kOffK + s * C::kKStage;
+          const uint32_t sK = sb + C::kOffK + s * C::kKStage, dS = tmem + kTmemS + 64 * s;
+          // one thread issues every product: its descriptors are the tiles'
+          // (built once here) advanced by constants, so the issue keeps pace
+          // with the tensor core
           if constexpr (Q8) {
             // e4m3 codes: 32 per product, two products per 64-byte block
-            const uint32_t sQ = sb + C::kOffQ8;
+            const uint64_t dq = sdesc_sw64(sb + C::kOffQ8, 16, 512), dk = sdesc_sw64(sK, 16, 512);
+#pragma unroll
             for (int k = 0; k < D / 32; ++k) {
               const uint32_t off = (uint32_t)(k & 1) * 32;
-              umma_ss_e4m3(tmem + kTmemS + 64 * s,
-                           sdesc_sw64(sQ + (k >> 1) * C::kBlkQ + off, 16, 512),
-                           sdesc_sw64(sK + (k >> 1) * C::kBlkK + off, 16, 512), idesc_qk,
+              umma_ss_e4m3(dS, sdesc_advance(dq, (k >> 1) * C::kBlkQ + off),
+                           sdesc_advance(dk, (k >> 1) * C::kBlkK + off), idesc_qk,
                            k > 0 ? 1u : 0u);
             }
           } else {
-            const uint32_t sQ = sb + C::kOffQ;
+            const uint64_t dq = sdesc_sw128(sb + C::kOffQ, 16, 1024), dk = sdesc_sw128(sK, 16, 1024);
+#pragma unroll
             for (int k = 0; k < D / 16; ++k) {
-              umma_ss(tmem + kTmemS + 64 * s,
-                      sdesc_sw128(sQ + (k >> 2) * kHalfQ + (k & 3) * 32, 16, 1024),
-                      sdesc_sw128(sK + (k >> 2) * kHalfKV + (k & 3) * 32, 16, 1024), idesc_qk,
+              umma_ss(dS, sdesc_advance(dq, (k >> 2) * kHalfQ + (k & 3) * 32),
+                      sdesc_advance(dk, (k >> 2) * kHalfKV + (k & 3) * 32), idesc_qk,
                       k > 0 ? 1u : 0u);
             }
           }
@@ -499,12 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar(kBarPReady + s), (tc >> 1) & 1, &s_abort)) return false;
           if (!mbar_wait(bar(kBarVReady + s), (tc >> 1) & 1, &s_abort)) return false;
           tc_fence_after();
-          const uint32_t sV = sb + C::kOffV + s * kOperand;
-          for (int k = 0; k < kN / 16; ++k) {
-            const uint64_t bd = sdesc_sw128(sV + k * 16 * 128, kHalfKV, 1024);
-            umma_ts(tmem + kTmemO, tmem + kTmemS + 64 * s + 8 * k, bd, idesc_pv,
+          const uint64_t dv = sdesc_sw128(sb + C::kOffV + s * kOperand, kHalfKV, 1024);
+          const uint32_t tP = tmem + kTmemS + 64 * s;
+#pragma unroll
+          for (int k = 0; k < kN / 16; ++k)
+            umma_ts(tmem + kTmemO, tP + 8 * k, sdesc_advance(dv, k * 16 * 128), idesc_pv,
                     (j > 0 || k > 0) ? 1u : 0u);
-          }
           umma_commit(bar(kBarVEmpty + s));
           umma_commit(bar(kBarPVDone));
           return true;

@@ -55,6 +55,15 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
+// The descriptor of the same tile layout starting `bytes` (a multiple of 16)
+// further on.  The start-address field holds the shared-memory address >> 4,
+// and a CTA's shared-memory addresses stay below 2^18, so the sum never
+// carries out of the field: a product's operand descriptor is its tile's,
+// built once, plus a constant.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B (or, with f16 = true,
 // fp16 A/B: both operands always share one type) and fp32 accumulate.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major,
