@@ -10,6 +10,9 @@
 //   O    columns [0, D)      fp32 accumulator of P V
 //   S_0  columns [256, 320)  scores of key tiles 0, 2, 4, ... (then P, bf16)
 //   S_1  columns [320, 384)  scores of key tiles 1, 3, 5, ...
+//   Q    columns [384, 384 + D/2)  the bf16 query tile, the A operand of S
+//        (placed by the softmax warps at the unit's start; with quantised
+//        queries S reads an e4m3 code tile from shared memory instead)
 // The MMA thread issues S(0), S(1), then per key tile j: P V(j), S(j+2).  So
 // the tensor core computes the scores of tile j+1 (and j+2) while the softmax
 // warpgroup works on tile j -- the overlap the RPA v3 kernel gets by
@@ -27,7 +30,8 @@
 // 64-column block of head_dim), the step's new keys [ctx, ...) from the
 // keys/values inputs (RPA v3 _fetch_bkv does the same).  Value rows no row
 // of the unit may see are zeroed before the P V product.  The unit's own new
-// tokens are written into their pages by the softmax warps.  With an e4m3
+// tokens are written into their pages by two otherwise idle warps while the
+// unit runs.  With an e4m3
 // cache the step's new tokens were written into their pages ahead of this
 // kernel, every tile comes from the pool, and the pages' codes land in a
 // staging buffer and are decoded into the operand stage: keys as bf16 (the
@@ -48,8 +52,8 @@ namespace rpa {
 namespace tcw {
 
 // warp 0: TMA (+ fp8 decoding); warp 1: MMA (one thread) and tensor-memory
-// allocation; warps 2-3: fp8 decoding (idle with a bf16 cache); warps 4-7:
-// softmax, one thread per row of the query tile
+// allocation; warps 2-3: fp8 decoding, or with a bf16 cache the unit's page
+// write; warps 4-7: softmax, one thread per row of the query tile
 constexpr int kThreads = 256;
 constexpr int kM = 128;                         // rows per unit (one query tile)
 constexpr int kN = 64;                          // keys per tile
@@ -57,6 +61,7 @@ constexpr uint32_t kHalfQ = 128 * 128;          // [128 rows][64 bf16], 16 KB
 constexpr uint32_t kHalfKV = 64 * 128;          // [64 rows][64 bf16], 8 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = 256;    // S slot b at kTmemS + 64 b
+constexpr uint32_t kTmemQ = 384;                // bf16 query tile (D/2 columns)
 constexpr int kRescaleLog2 = 8;
 
 // With quantised queries (Q8) the query tile and the key stages are e4m3 code
@@ -94,17 +99,19 @@ __device__ __forceinline__ uint32_t sw64_codes(int r, int c8) {
 enum Bar {
   kBarQFull = 0,    // the query tile landed
   kBarKFull = 1,    // [2] key TMA landed
-  kBarKEmpty = 3,   // [2] key stage free (its S product done)
+  kBarKEmpty = 3,   // [2] unused: a key stage is free once its S product is done (kBarSFull)
   kBarVFull = 5,    // [2] value TMA landed
   kBarVReady = 7,   // [2] values fixed up / decoded, MMA may read
-  kBarVEmpty = 9,   // [2] value stage free (its P V product done)
+  kBarVEmpty = 9,   // [2] value stage free: its P V product done (every P V product
+                    // completes one of the two in turn, which also orders O rescales)
   kBarKReady = 11,  // [2] fp8 cache: keys decoded, MMA may read
-  kBarSFull = 13,   // [2] per S slot: S computed
+  kBarSFull = 13,   // [2] per S slot: S computed (and its key stage free)
   kBarPReady = 15,  // [2] per S slot: P written (and O corrected)
-  kBarPVDone = 17,  // every P V product done, in order (for O rescales)
+  kBarPVDone = 17,  // unused (kBarVEmpty)
   kBarODone = 18,   // the unit's last P V product done
   kBarDrain = 19,   // once, at exit: every tcgen05 product the MMA thread issued is done
-  kBarQReady = 20,  // quantised queries (q_scale): the softmax warps converted the tile
+  kBarQReady = 20,  // the softmax warps placed the query tile: in tensor memory (bf16),
+                    // or as its e4m3 code tile (quantised queries, q_scale)
   kNumBars = 21,
 };
 
@@ -208,7 +215,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarQFull), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
-      mbar_init(bar(kBarKEmpty + s), 1);
       mbar_init(bar(kBarVFull + s), 1);
       mbar_init(bar(kBarVReady + s), FP8 ? kDecWarps : 1);
       mbar_init(bar(kBarVEmpty + s), 1);
@@ -216,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarPReady + s), 4);
     }
-    mbar_init(bar(kBarPVDone), 1);
     mbar_init(bar(kBarODone), 1);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarQReady), 4);
@@ -411,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ids_j = load_ids(0);
         int ids_j1 = nt > 1 ? load_ids(1) : 0;
         if (nt >= 1) {
-          if (!mbar_wait_warp(bar(kBarKEmpty + (tcount & 1)), ((tcount >> 1) & 1) ^ 1, &s_abort))
+          if (!mbar_wait_warp(bar(kBarSFull + (tcount & 1)), ((tcount >> 1) & 1) ^ 1, &s_abort))
             ok = false;
           else {
             issue(0, 0, tcount, ids_j);
@@ -423,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = tc & 1;
           if (j + 1 < nt) {
             const uint32_t tn = tc + 1;
-            if (!mbar_wait_warp(bar(kBarKEmpty + (tn & 1)), ((tn >> 1) & 1) ^ 1, &s_abort)) {
+            if (!mbar_wait_warp(bar(kBarSFull + (tn & 1)), ((tn >> 1) & 1) ^ 1, &s_abort)) {
               ok = false;
               break;
             }
@@ -465,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                mbar_wait_warp(bar(kBarKReady + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort);
           if (!ok) break;
         }
-        if (!mbar_wait_warp(bar(kBarKEmpty + s), par, &s_abort)) {
+        if (!mbar_wait_warp(bar(kBarSFull + s), par, &s_abort)) {
           ok = false;
           break;
         }
@@ -510,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S(0), S(1), then per tile j: P V(j), S(j+2).  Key stage and S slot
       // of tile j are both (tcount + j) & 1.
       if (lane == 0) {
-        bool ok = mbar_wait(bar(Q8 ? kBarQReady : kBarQFull), ucount & 1, &s_abort);
+        bool ok = mbar_wait(bar(kBarQReady), ucount & 1, &s_abort);
         tc_fence_after();
         auto qk = [&](uint32_t tc) -> bool {
           const int s = tc & 1;
@@ -532,16 +537,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                            k > 0 ? 1u : 0u);
             }
           } else {
-            const uint64_t dq = sdesc_sw128(sb + C::kOffQ, 16, 1024), dk = sdesc_sw128(sK, 16, 1024);
+            // bf16 queries from tensor memory (16 of D per product = 8
+            // columns), keys from the stage: only the keys cross the
+            // shared-memory port
+            const uint64_t dk = sdesc_sw128(sK, 16, 1024);
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              umma_ss(dS, sdesc_advance(dq, (k >> 2) * kHalfQ + (k & 3) * 32),
+            for (int k = 0; k < D / 16; ++k)
+              umma_ts(dS, tmem + kTmemQ + 8 * k,
                       sdesc_advance(dk, (k >> 2) * kHalfKV + (k & 3) * 32), idesc_qk,
                       k > 0 ? 1u : 0u);
-            }
           }
-          umma_commit(bar(kBarSFull + s));
-          umma_commit(bar(kBarKEmpty + s));
+          umma_commit(bar(kBarSFull + s));  // S ready, and the key stage free
           return true;
         };
         auto pv = [&](uint32_t tc, int j) -> bool {
@@ -555,8 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kN / 16; ++k)
             umma_ts(tmem + kTmemO, tP + 8 * k, sdesc_advance(dv, k * 16 * 128), idesc_pv,
                     (j > 0 || k > 0) ? 1u : 0u);
-          umma_commit(bar(kBarVEmpty + s));
-          umma_commit(bar(kBarPVDone));
+          umma_commit(bar(kBarVEmpty + s));  // value stage free, O holds P V(j)
           return true;
         };
         if (ok && nt >= 1) ok = qk(tcount);
@@ -603,7 +608,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       });
     } else {
-      unit_loop([](const Geom&, uint32_t, uint32_t) {});
+      // bf16 cache: warps 2 and 3 write this unit's new tokens into their
+      // pages, half of them each, while the other roles run the unit (no
+      // tile of this step reads those slots: the unit's new keys and values
+      // come from the inputs, and the pool's tiles end at the step's
+      // context).  An e4m3 cache had them written ahead of this kernel.
+      unit_loop([&](const Geom& g, uint32_t, uint32_t) {
+        const int n = g.t_end - g.t_begin, w = warp - 2;
+        const int i0 = n * w / 2, i1 = n * (w + 1) / 2;
+        write_tokens_kv<FP8, D, 4>(a.kv, g.seq, g.q0 + g.t_begin + i0, g.ctx + g.t_begin + i0,
+                                   i1 - i0, g.h, lane);
+      });
     }
   } else {
     unit_loop([&](const Geom& g, const uint32_t tcount, const uint32_t ucount) {
@@ -618,17 +633,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = g.ctx + i_tok;
       const int hq = g.h * G + r % G;
       const uint32_t tO = tmem + lane_off + kTmemO;
-      if constexpr (Q8) {
+      if (!mbar_wait_warp(bar(kBarQFull), ucount & 1, &s_abort)) {
+        if (lane == 0) {
+          set_status(hdr, RPA_STATUS_TIMEOUT);
+          s_abort = 1;
+        }
+        return;
+      }
+      if constexpr (!Q8) {
+        // the query tile into tensor memory, the A operand of S: each thread
+        // moves its own row (lane r of the tile), 64 elements (32 columns)
+        // at a time; the previous unit's products are all done (its O was
+        // read), so the columns are free
+#pragma unroll 1
+        for (int hf = 0; hf < C::kHalves; ++hf) {
+          uint32_t qv[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(smem + C::kOffQ + hf * kHalfQ + sw128(r, c));
+            qv[4 * c] = v.x;
+            qv[4 * c + 1] = v.y;
+            qv[4 * c + 2] = v.z;
+            qv[4 * c + 3] = v.w;
+          }
+          tmem_st32p(tmem + lane_off + kTmemQ + 32 * hf, qv);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQReady));
+      } else {
         // quantised queries: the four softmax warps turn the bf16 query tile
         // into its e4m3 code tile (q / q_scale rounded to e4m3) before the MMA
         // thread reads it
-        if (!mbar_wait_warp(bar(kBarQFull), ucount & 1, &s_abort)) {
-          if (lane == 0) {
-            set_status(hdr, RPA_STATUS_TIMEOUT);
-            s_abort = 1;
-          }
-          return;
-        }
         constexpr int kChunks = D / 8;  // 8 elements per chunk
         for (int i = tid - 128; i < kM * kChunks; i += 128) {
           const int rr = i / kChunks, c = i % kChunks;
@@ -640,15 +677,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarQReady));
-      }
-
-      // this unit's new tokens -> their pages, a quarter of them per warp
-      // (an e4m3 cache had them written ahead of this kernel)
-      if constexpr (!FP8) {
-        const int n = g.t_end - g.t_begin, w = warp - 4;
-        const int i0 = n * w / 4, i1 = n * (w + 1) / 4;
-        write_tokens_kv<FP8, D, 2>(a.kv, g.seq, g.q0 + g.t_begin + i0, g.ctx + g.t_begin + i0,
-                                   i1 - i0, g.h, lane);
       }
 
       float m_run = a.sink ? a.sink[hq] * kLog2e : -INFINITY;
@@ -704,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // O holds P V of tiles < j once P V(j-1) is done: S(j) may have
           // completed before it, so wait for that product first
-          if (!mbar_wait_warp(bar(kBarPVDone), (tc - 1) & 1, &s_abort)) {
+          if (!mbar_wait_warp(bar(kBarVEmpty + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, &s_abort)) {
             ok = false;
             break;
           }
