@@ -80,6 +80,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait without suspending: polls the barrier with test_wait (checking
+// the abort flag and the time limit every 64 polls).  For a lone thread
+// whose waits are short and on the critical path (the MMA-issuing thread of
+// the prefill), where waking from a suspended try_wait costs more than the
+// polling takes from the warps sharing its scheduler.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity,
+                                               volatile int* abort) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
 // mbar_wait for a whole warp (all 32 lanes call it): every lane returns from
 // its own bounded wait, then the warp agrees on one outcome.  Lanes that saw
 // the abort flag at different moments would otherwise leave their loop

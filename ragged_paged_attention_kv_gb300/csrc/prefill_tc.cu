@@ -532,12 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and its completion also tells the softmax of tile X that PV_X(j) is
       // done, so O_X may be rescaled.
       if (lane == 0) {
-        bool ok = mbar_wait(bar(Q8 ? kBarQReady : kBarQFull), ucount & 1, &s_abort);
+        bool ok = mbar_wait_poll(bar(Q8 ? kBarQReady : kBarQFull), ucount & 1, &s_abort);
         tc_fence_after();
         auto qk = [&](uint32_t tc, int x, bool last_of_stage) -> bool {
           const int s = tc & 1;
           if (x == 0) {
-            if (!mbar_wait(bar((FP8 ? kBarKReady : kBarKFull) + s), (tc >> 1) & 1, &s_abort))
+            if (!mbar_wait_poll(bar((FP8 ? kBarKReady : kBarKFull) + s), (tc >> 1) & 1,
+                                &s_abort))
               return false;
             tc_fence_after();
           }
@@ -570,8 +571,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto pv = [&](uint32_t tc, int j, int x, bool last_of_stage) -> bool {
           const int s = tc & 1;
-          if (!mbar_wait(bar(kBarPReady + x), (n.tiles(x) + j) & 1, &s_abort)) return false;
-          if (x == 0 && !mbar_wait(bar(kBarVReady + s), (tc >> 1) & 1, &s_abort)) return false;
+          if (!mbar_wait_poll(bar(kBarPReady + x), (n.tiles(x) + j) & 1, &s_abort)) return false;
+          if (x == 0 && !mbar_wait_poll(bar(kBarVReady + s), (tc >> 1) & 1, &s_abort))
+            return false;
           tc_fence_after();
           const uint64_t dv = sdesc_sw128(sb + kOffV + s * kOperand, kHalf, 1024);
           const uint32_t tO = tmem + kTmemO + 128 * x, tP = tmem + kTmemS + 128 * x;
