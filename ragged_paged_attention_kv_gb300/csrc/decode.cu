@@ -36,19 +36,21 @@ constexpr int kRescaleLog2 = 8;               // lazy-rescale threshold (log2 un
 
 template <int D, bool FP8>
 struct Cfg {
-  // Two CTAs per SM put two consumer warps on each scheduler, so one warp's
-  // ldmatrix -> MMA -> softmax chain hides behind the other's, and double the
-  // units in flight when short units make the path latency-bound.  head_dim
-  // 64 fits them outright; bf16 head_dim 128 fits in 168 registers (12 bytes
-  // of spills) and two 32 KB stages per CTA (128 KB in flight per SM), and
-  // runs 4 % faster than one CTA with five stages.  fp8 at 128 (more
-  // conversion registers) and head_dim 256 keep one CTA per SM.
+  // Several CTAs per SM put several consumer warps on each scheduler, so one
+  // warp's ldmatrix -> MMA -> softmax chain hides behind another's, and
+  // multiply the units in flight when short units make the path
+  // latency-bound.  head_dim 64 runs three (128 registers; the e4m3 kernel
+  // spills 16 bytes; four, at 96 registers, spilled 92 bytes and ran 16 %
+  // slower); bf16 head_dim 128 runs two in 168 registers (12 bytes of spills)
+  // with two 32 KB stages per CTA (128 KB in flight per SM), 4 % faster than
+  // one CTA with five stages.  fp8 at 128 (more conversion registers) and
+  // head_dim 256 keep one CTA per SM.
   // head_dim 96 runs as 128 in shared memory (a multiple of 64 columns):
   // past the real row, bf16 stages hold TMA's zero fill and fp8 ones the
   // conversion's zeros; the query rows land at the padded stride; only the
   // real columns are read from or written to global memory
   static constexpr int kDp = (D + 63) / 64 * 64;
-  static constexpr int kCtasPerSm = (kDp == 64 || (kDp == 128 && !FP8)) ? 2 : 1;
+  static constexpr int kCtasPerSm = kDp == 64 ? 3 : ((kDp == 128 && !FP8) ? 2 : 1);
   // bytes of one box row in smem: an fp8 stage keeps the real head_dim (the
   // conversion to the padded bf16 operand zero-fills the rest)
   static constexpr int kRowBytes = FP8 ? D : 128;
@@ -70,7 +72,8 @@ struct Cfg {
   static constexpr int kMergeBytes = kConsumerWarps * kDecodeRows * (kDp + 2) * 4;
   // as many stages as fit next to the other buffers (at most 12, 160 KB)
   static constexpr int kBudget =
-      (kCtasPerSm == 2 ? 110 : 220) * 1024 - 2 * kQBytes - kConvBytes - kMergeBytes - 1024 - 256;
+      (kCtasPerSm == 3 ? 72 : kCtasPerSm == 2 ? 110 : 220) * 1024 - 2 * kQBytes - kConvBytes -
+      kMergeBytes - 1024 - 256;
   static constexpr int kStages1 = (kBudget < 160 * 1024 ? kBudget : 160 * 1024) / kStageBytes;
   static constexpr int kStages = kStages1 > 12 ? 12 : (kStages1 < 2 ? 2 : kStages1);
   // layout: [stages][q slots 2][conv][merge][unit info 2][barriers]
