@@ -312,6 +312,24 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// lo += the low 16-bit value of pk, hi += the high one: bf16 (or fp16 with
+// F16) values converted exactly to fp32 inside a mixed-precision add, one
+// instruction each (no separate unpacking).
+template <bool F16>
+__device__ __forceinline__ void add_halves_f32(float& lo, float& hi, uint32_t pk) {
+  if constexpr (F16) {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n add.rn.f32.f16 %0, l, %0;\n"
+        " add.rn.f32.f16 %1, h, %1;\n}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(pk));
+  } else {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n add.rn.f32.bf16 %0, l, %0;\n"
+        " add.rn.f32.bf16 %1, h, %1;\n}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(pk));
+  }
+}
+
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

@@ -766,25 +766,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the row sum adds exactly the rounded weights just stored; it is
         // formed after P is handed over, off the tensor core's wait
         {
-          uint64_t rs2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+          float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c = 0; c < kN / 2; ++c) {
-            const uint32_t pk = sr[c];
-            float r0, r1;
-            if (FP8) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk));
-              r0 = f.x;
-              r1 = f.y;
-            } else {
-              r0 = __uint_as_float(pk << 16);
-              r1 = __uint_as_float(pk & 0xFFFF0000u);
-            }
-            rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(r0, r1));
-          }
-          float a0, a1, b0, b1;
-          f2_unpack(rs2[0], a0, a1);
-          f2_unpack(rs2[1], b0, b1);
-          l_run += (a0 + a1) + (b0 + b1);
+          for (int c = 0; c < kN / 2; ++c)
+            add_halves_f32<FP8>(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], sr[c]);
+          l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
         }
       }
       // epilogue: O / l -> bf16 rows
