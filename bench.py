@@ -281,7 +281,7 @@ def launches_per_step(w):
 BOUNDS = {
     "decode": "hbm",
     "decode_d256": "hbm",
-    "mixed": "hbm (decode share) + tensor (prefill share); the decode kernel runs on 9/16 of "
+    "mixed": "hbm (decode share) + tensor (prefill share); the decode kernel runs on 80 of 152 "
              "the SMs while the prefill kernel starts on the rest, so its time alone (kernel "
              "events) is longer than its share of the overlapped step",
     "long": "tensor",

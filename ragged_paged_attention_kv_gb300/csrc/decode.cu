@@ -139,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
   griddep_launch_dependents();
   if (hdr[kHdrNumDecode] == 0) return;  // a prefill-only batch: nothing to set up
   // A batch with enough prefill work as well (the planner's decision): the
-  // CTAs on 7 of every 16 SMs leave at once, so the prefill kernel's CTAs,
+  // CTAs on 8 of every 16 SMs (by %smid: 72 of the 152) leave at once, so
+  // the prefill kernel's CTAs,
   // launched behind this grid and waiting for no part of it, run there from
   // the start while the decode stays HBM-bound on the other SMs.  Only with
   // more CTAs than the leaving SMs can hold, so that some always stay: the
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, FP8>::kCtasPerSm)
   if (hdr[kHdrDecodeShare] && gridDim.x > 72 * C::kCtasPerSm) {
     uint32_t smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    if ((smid & 15u) >= 9u) return;
+    if ((smid & 15u) >= 8u) return;
   }
 
   // zero both query slots (rows >= G stay zero), init barriers; the bulk

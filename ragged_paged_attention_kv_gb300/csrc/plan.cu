@@ -25,7 +25,7 @@ constexpr int kSizeClasses = 16;  // decode sequences are ordered by these, long
 // (the decode kernel's CTAs on the other SMs leave at once) and the prefill
 // kernel's CTAs, launched behind it and waiting for no part of it, on the
 // rest from the start: the decode stays HBM-bound on fewer SMs (measured on
-// GB300: 9/16 of the SMs keep about 80 % of its bandwidth) while the prefill
+// GB300: 80 of the 152 SMs keep about 70 % of its bandwidth) while the prefill
 // is bound by the tensor cores.  Only worth it when the prefill is big enough
 // to keep the freed SMs busy: at least kShareFlopsPerByte prefill flops per
 // byte of keys / values the decode reads (the chunked-prefill mixed batch has
