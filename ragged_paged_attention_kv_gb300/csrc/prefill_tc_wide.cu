@@ -99,20 +99,18 @@ __device__ __forceinline__ uint32_t sw64_codes(int r, int c8) {
 enum Bar {
   kBarQFull = 0,    // the query tile landed
   kBarKFull = 1,    // [2] key TMA landed
-  kBarKEmpty = 3,   // [2] unused: a key stage is free once its S product is done (kBarSFull)
-  kBarVFull = 5,    // [2] value TMA landed
-  kBarVReady = 7,   // [2] values fixed up / decoded, MMA may read
-  kBarVEmpty = 9,   // [2] value stage free: its P V product done (every P V product
+  kBarVFull = 3,    // [2] value TMA landed
+  kBarVReady = 5,   // [2] values fixed up / decoded, MMA may read
+  kBarVEmpty = 7,   // [2] value stage free: its P V product done (every P V product
                     // completes one of the two in turn, which also orders O rescales)
-  kBarKReady = 11,  // [2] fp8 cache: keys decoded, MMA may read
-  kBarSFull = 13,   // [2] per S slot: S computed (and its key stage free)
-  kBarPReady = 15,  // [2] per S slot: P written (and O corrected)
-  kBarPVDone = 17,  // unused (kBarVEmpty)
-  kBarODone = 18,   // the unit's last P V product done
-  kBarDrain = 19,   // once, at exit: every tcgen05 product the MMA thread issued is done
-  kBarQReady = 20,  // the softmax warps placed the query tile: in tensor memory (bf16),
+  kBarKReady = 9,   // [2] fp8 cache: keys decoded, MMA may read
+  kBarSFull = 11,   // [2] per S slot: S computed (and its key stage free)
+  kBarPReady = 13,  // [2] per S slot: P written (and O corrected)
+  kBarODone = 15,   // the unit's last P V product done
+  kBarDrain = 16,   // once, at exit: every tcgen05 product the MMA thread issued is done
+  kBarQReady = 17,  // the softmax warps placed the query tile: in tensor memory (bf16),
                     // or as its e4m3 code tile (quantised queries, q_scale)
-  kNumBars = 21,
+  kNumBars = 18,
 };
 
 struct Maps {
