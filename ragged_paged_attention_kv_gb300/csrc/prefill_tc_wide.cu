@@ -31,16 +31,14 @@
 // keys/values inputs (RPA v3 _fetch_bkv does the same).  Value rows no row
 // of the unit may see are zeroed before the P V product.  The unit's own new
 // tokens are written into their pages by two otherwise idle warps while the
-// unit runs.  With an e4m3
-// cache the step's new tokens were written into their pages ahead of this
-// kernel, every tile comes from the pool, and the pages' codes land in a
-// staging buffer and are decoded into the operand stage: keys as bf16 (the
-// queries' type), values as fp16 (exact for e4m3), with P packed as fp16 to
-// match.  With quantised queries (q_scale)
-// S = Q K^T runs on the e4m3 codes themselves (tcgen05.mma kind::f8f6f4):
-// the query tile is quantised once per unit into a code tile, key pages land
-// as codes in code-tile key stages, and the logit scale carries
-// q_scale * k_scale.
+// unit runs.  With an e4m3 cache the step's new tokens were written into
+// their pages ahead of this kernel, every tile comes from the pool, and the
+// pages' codes land in a staging buffer and are decoded into the operand
+// stage: keys as bf16 (the queries' type), values as fp16 (exact for e4m3),
+// with P packed as fp16 to match.  With quantised queries (q_scale) S = Q K^T
+// runs on the e4m3 codes themselves (tcgen05.mma kind::f8f6f4): the query
+// tile is quantised once per unit into a code tile, key pages land as codes
+// in code-tile key stages, and the logit scale carries q_scale * k_scale.
 #include "async.cuh"
 #include "common.cuh"
 #include "kv_write.cuh"
